@@ -1,0 +1,241 @@
+/*
+ * moe.h - C ABI of libmoe: the forward pass of one DeepSeekMoE layer on one
+ * NVIDIA B300 (sm_103a).
+ *
+ * The layer is the one of the "DeepSeek-V3 Technical Report":
+ *   - DeepSeekMoE paragraph: token t's FFN output is the sum of N_s shared
+ *     experts plus the gate-weighted outputs of K routed experts; the
+ *     affinity of token t to routed expert i is sigmoid(u_t . e_i) and the
+ *     gates are the selected affinities normalised among themselves;
+ *   - auxiliary-loss-free load balancing paragraph: a per-expert bias b_i is
+ *     added to the affinity only to choose the top-K; after each step b_i
+ *     goes down by gamma if expert i was overloaded, up by gamma otherwise;
+ *     node-limited routing (here: group-limited); no token is dropped;
+ *   - fine-grained quantisation and increased-precision accumulation
+ *     paragraphs, Appendix B.2: FP8 E4M3 with one scale per 1 x 128
+ *     activation tile and per 128 x 128 weight block, FP32 accumulation.
+ *
+ * One call per step of the layer:
+ *     moe_route -> moe_permute -> moe_experts_grouped -> moe_combine
+ *               -> moe_bias_update
+ *
+ * Conventions shared by every call
+ *   - All tensors are dense, row-major, in device memory allocated and owned
+ *     by the caller.  The library allocates no memory and keeps no state
+ *     between calls except a per-device 32-bit error word.
+ *   - Every call enqueues its kernels on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and returns without synchronising.  The
+ *     host never learns the per-expert loads: every kernel reads them from
+ *     device memory.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     failed check returns an error status and launches nothing.
+ *   - Faults found on the device (a wait that timed out, an index out of
+ *     range) never trap: they set bits in the error word, which
+ *     moe_get_device_error() reads and clears.
+ *   - Pointers must be 16-byte aligned.  For the BF16 and FP8 kinds, d and
+ *     I must be multiples of 128.
+ *   - Results are deterministic: the same inputs give bitwise-identical
+ *     outputs (no atomics decide any output order or floating-point sum).
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Arithmetic kind of the expert path. */
+typedef enum {
+  MOE_DTYPE_FP32 = 0,     /* x, weights, intermediates and output in fp32 */
+  MOE_DTYPE_BF16 = 1,     /* x, weights, h, y in bf16; fp32 accumulation  */
+  MOE_DTYPE_FP8_E4M3 = 2  /* x in bf16, quantised to E4M3 per 1x128 tile;
+                             weights E4M3 + fp32 128x128 block scales;
+                             fp32 accumulation; bf16 output              */
+} moe_dtype_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer or inconsistent configuration */
+  MOE_ERR_SHAPE = 2,        /* size outside what a kernel supports          */
+  MOE_ERR_ALIGN = 3,        /* pointer not 16-byte aligned                  */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call failed                   */
+  MOE_ERR_TIMEOUT = 5,      /* a device wait gave up (error word)           */
+  MOE_ERR_DEVICE = 6,       /* another device-side check failed             */
+  MOE_ERR_WORKSPACE = 7     /* workspace smaller than moe_workspace_bytes   */
+} moe_status_t;
+
+/* Shape of one layer.  Symbols of the DeepSeekMoE paragraph: N_r = E routed
+ * experts, K_r = K active per token, N_s = n_shared; node-limited routing
+ * reads as n_groups contiguous groups of E / n_groups experts of which a
+ * token may use topk_groups. */
+typedef struct {
+  int32_t T;                /* tokens in the batch                          */
+  int32_t d;                /* hidden size (FFN input/output width)         */
+  int32_t E;                /* routed experts                               */
+  int32_t n_groups;         /* expert groups (E % n_groups == 0)            */
+  int32_t topk_groups;      /* groups a token may use                       */
+  int32_t K;                /* routed experts per token                     */
+  int32_t n_shared;         /* shared experts (0 allowed)                   */
+  int32_t inter;            /* intermediate size I of every expert          */
+  int32_t group_score_topn; /* a group's score: sum of its top-n biased
+                               affinities (2 in the DeepSeek-V3 reading)    */
+  float route_scale;        /* rho: gates sum to rho for every token        */
+  float gamma;              /* bias update speed                            */
+  int32_t dtype;            /* moe_dtype_t                                  */
+} moe_cfg_t;
+
+/* Human-readable name of a status. */
+const char* moe_status_str(moe_status_t status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int32_t moe_version(void);
+
+/* Checks a configuration: MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_SHAPE.
+ * Limits: 1 <= T <= 2^22; 1 <= E <= 1024; 1 <= K <= min(32, E);
+ * n_groups divides E; 1 <= topk_groups <= n_groups <= 32; the kept groups
+ * hold at least K experts; 1 <= group_score_topn; d, inter >= 1. */
+moe_status_t moe_check_cfg(const moe_cfg_t* cfg);
+
+/* Bytes of scratch memory that moe_route and moe_experts_grouped need for
+ * this configuration (one buffer serves both; contents need not survive
+ * between calls).  0 for an invalid configuration. */
+size_t moe_workspace_bytes(const moe_cfg_t* cfg);
+
+/*
+ * moe_route - affinities, group-limited top-K, gates, per-expert segments.
+ *
+ * DeepSeekMoE paragraph (sigmoid affinity, gates normalised among the
+ * selected affinities) and auxiliary-loss-free paragraph (bias for the
+ * choice only; no token dropped).
+ *
+ *   x            [T, d]   fp32 (FP32 kind) or bf16 (BF16 / FP8 kinds)
+ *   router_w     [E, d]   fp32 centroids e_i (routing stays in fp32)
+ *   bias         [E]      fp32 b_i
+ *   affinity_in  [T, E]   fp32, nullable: when given, these affinities are
+ *                         used as s and the router product is skipped
+ *   affinity_out [T, E]   fp32, nullable: receives s = sigmoid(x e^T)
+ *   topk_idx     [T, K]   int32 out: chosen experts by descending biased
+ *                         score fl32(s + b), ties to the lower index
+ *   topk_w       [T, K]   fp32 out: rho * s / sum of the chosen s
+ *   counts       [E]      int32 out: tokens routed to each expert
+ *   offsets      [E + 1]  int32 out: exclusive prefix sum of counts
+ *   row_of_slot  [T, K]   int32 out: permuted row of token t's k-th copy
+ *   token_of_row [T * K]  int32 out: token copied into each permuted row;
+ *                         inside an expert's segment rows follow ascending
+ *                         token index
+ *   ws, ws_bytes          scratch, at least moe_workspace_bytes(cfg)
+ *
+ * Group score: the fp32 sum, in descending order, of the group's top
+ * group_score_topn biased scores; groups are kept by descending score,
+ * ties to the lower group index.  Bit-exact given the same fp32 s.
+ */
+moe_status_t moe_route(const moe_cfg_t* cfg, const void* x, const float* router_w,
+                       const float* bias, const float* affinity_in,
+                       float* affinity_out, int32_t* topk_idx, float* topk_w,
+                       int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
+                       int32_t* token_of_row, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/*
+ * moe_permute - copy every token row into its experts' segments
+ * (the single-device form of the dispatch of the cross-node all-to-all
+ * paragraph).
+ *
+ *   x             [T, d]      fp32 / bf16 input rows
+ *   token_of_row  [T * K]     from moe_route
+ *   x_perm        [T * K, d]  out: FP32 kind fp32, BF16 kind bf16, FP8 kind
+ *                             E4M3 bytes (row r = x[token_of_row[r]])
+ *   x_perm_scales [T * K, d/128] fp32 out, FP8 kind only (else NULL): the
+ *                 1 x 128 tile scales fl32(amax / 448), 1 for a zero tile
+ *   x_q, x_q_scales  FP8 kind only (else NULL): [T, d] E4M3 and
+ *                 [T, d/128] fp32 - each token quantised once, before the
+ *                 copies ("dispatch activations in FP8"); the shared expert
+ *                 reads them too
+ */
+moe_status_t moe_permute(const moe_cfg_t* cfg, const void* x,
+                         const int32_t* token_of_row, void* x_perm,
+                         float* x_perm_scales, void* x_q, float* x_q_scales,
+                         void* stream);
+
+/*
+ * moe_experts_grouped - every routed expert's SwiGLU FFN on its segment,
+ * plus the shared experts on all T tokens.
+ *
+ * DeepSeekMoE paragraph (fine-grained routed experts and shared experts;
+ * every expert is W2 (silu(W1 u) * (W3 u))).
+ *
+ *   x_perm, x_perm_scales  from moe_permute (scales: FP8 kind only)
+ *   x, x_scales   [T, d] shared-expert input rows: the layer input (FP32 /
+ *                 BF16 kinds; x_scales NULL) or moe_permute's x_q and
+ *                 x_q_scales (FP8 kind)
+ *   offsets       [E + 1] from moe_route
+ *   w13           [E, 2I, d] rows [0, I) = W1 (gate), [I, 2I) = W3 (up)
+ *   w2            [E, d, I]
+ *   ws13, ws2     [N_s, 2I, d], [N_s, d, I] shared experts (NULL if N_s = 0)
+ *   *_scales      FP8 kind: fp32 block scales of the weight above it,
+ *                 [E, 2I/128, d/128], [E, d/128, I/128], [N_s, ...]
+ *                 (see moe_quantize_weights_fp8); NULL otherwise
+ *   y_perm        [T * K, d] out: expert output of every permuted row
+ *                 (fp32 for the FP32 kind, else bf16)
+ *   y_shared      [T, d] out: sum of the shared experts' outputs (NULL
+ *                 if N_s = 0)
+ *
+ * The N_s shared experts are evaluated as one expert of intermediate size
+ * N_s * I (the same sum, in one fp32 accumulator).
+ */
+moe_status_t moe_experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
+                                 const float* x_perm_scales, const void* x,
+                                 const float* x_scales, const int32_t* offsets,
+                                 const void* w13, const float* w13_scales,
+                                 const void* w2, const float* w2_scales,
+                                 const void* ws13, const float* ws13_scales,
+                                 const void* ws2, const float* ws2_scales,
+                                 void* y_perm, void* y_shared, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/*
+ * moe_combine - gate-weighted un-permute:
+ *   out[t] = y_shared[t] + sum_{k < K} topk_w[t, k] * y_perm[row_of_slot[t, k]]
+ * summed in fp32 in exactly that order (DeepSeekMoE paragraph).
+ *
+ *   y_perm [T*K, d], y_shared [T, d] (nullable): fp32 (FP32 kind) or bf16
+ *   out    [T, d] fp32 (FP32 kind) or bf16
+ */
+moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y_perm,
+                         const void* y_shared, const int32_t* row_of_slot,
+                         const float* topk_w, void* out, void* stream);
+
+/*
+ * moe_bias_update - the sign rule of the auxiliary-loss-free paragraph:
+ *   b_i <- fl32(b_i - gamma) if counts_i * E > T * K   (overloaded)
+ *   b_i <- fl32(b_i + gamma) otherwise
+ *   counts [E] int32 (from moe_route), bias [E] fp32 in/out.
+ */
+moe_status_t moe_bias_update(const moe_cfg_t* cfg, const int32_t* counts,
+                             float* bias, void* stream);
+
+/*
+ * moe_quantize_weights_fp8 - offline utility: quantise `n_mats` bf16
+ * matrices [rows, cols] (contiguous, cols % 128 == 0) to E4M3 in 128 x 128
+ * blocks (fine-grained quantisation paragraph): scale = fl32(amax / 448)
+ * (1 for a zero block), code = E4M3(fl32(w / scale)), round to nearest
+ * even, saturating.  q [n_mats, rows, cols] bytes; scales
+ * [n_mats, ceil(rows/128), cols/128] fp32.
+ */
+moe_status_t moe_quantize_weights_fp8(const void* w_bf16, int32_t n_mats,
+                                      int32_t rows, int32_t cols, void* q,
+                                      float* scales, void* stream);
+
+/* Synchronises `stream`, returns the device error word (MOE_OK if clear,
+ * MOE_ERR_TIMEOUT if a wait gave up, MOE_ERR_DEVICE for any other device
+ * check) and clears it. */
+moe_status_t moe_get_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,237 @@
+"""DeepSeekMoE layer forward on one B300 (sm_103a): Python binding of libmoe.
+
+The binding only marshals arguments: every step of the layer runs in the
+CUDA kernels of ``libmoe.so`` (built in-tree by ``build.py``).  PyTorch
+provides device memory and streams.  Importing this package fails loudly if
+the shared library is missing: there is no CPU fallback.
+
+Calls (same names as the C ABI in include/moe.h):
+    moe_route, moe_permute, moe_experts_grouped, moe_combine,
+    moe_bias_update, moe_quantize_weights_fp8, moe_get_device_error,
+    moe_workspace_bytes, moe_check_cfg
+and ``MoELayer``, which owns the buffers of one layer and runs the five
+calls of a forward step in order on one stream.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m mixture_experts_layer_82_b300.build`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+DTYPE_FP32, DTYPE_BF16, DTYPE_FP8_E4M3 = 0, 1, 2
+_DTYPES = {"fp32": DTYPE_FP32, "bf16": DTYPE_BF16, "fp8": DTYPE_FP8_E4M3}
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_ALIGN",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE",
+          7: "MOE_ERR_WORKSPACE"}
+
+EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_bytes",
+            "moe_route", "moe_permute", "moe_experts_grouped", "moe_combine",
+            "moe_bias_update", "moe_quantize_weights_fp8", "moe_get_device_error")
+
+
+class MoeCfg(ctypes.Structure):
+    """Mirror of moe_cfg_t."""
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("group_score_topn", ctypes.c_int32), ("route_scale", ctypes.c_float),
+                ("gamma", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)} "
+                         f"({_lib.moe_status_str(status).decode()})")
+
+
+_P = ctypes.c_void_p
+_CFG = ctypes.POINTER(MoeCfg)
+_lib.moe_status_str.restype = ctypes.c_char_p
+_lib.moe_status_str.argtypes = [ctypes.c_int]
+_lib.moe_version.restype = ctypes.c_int32
+_lib.moe_version.argtypes = []
+_lib.moe_check_cfg.restype = ctypes.c_int
+_lib.moe_check_cfg.argtypes = [_CFG]
+_lib.moe_workspace_bytes.restype = ctypes.c_size_t
+_lib.moe_workspace_bytes.argtypes = [_CFG]
+_lib.moe_route.restype = ctypes.c_int
+_lib.moe_route.argtypes = [_CFG] + [_P] * 11 + [_P, ctypes.c_size_t, _P]
+_lib.moe_permute.restype = ctypes.c_int
+_lib.moe_permute.argtypes = [_CFG] + [_P] * 6 + [_P]
+_lib.moe_experts_grouped.restype = ctypes.c_int
+_lib.moe_experts_grouped.argtypes = [_CFG] + [_P] * 15 + [_P, ctypes.c_size_t, _P]
+_lib.moe_combine.restype = ctypes.c_int
+_lib.moe_combine.argtypes = [_CFG] + [_P] * 5 + [_P]
+_lib.moe_bias_update.restype = ctypes.c_int
+_lib.moe_bias_update.argtypes = [_CFG, _P, _P, _P]
+_lib.moe_quantize_weights_fp8.restype = ctypes.c_int
+_lib.moe_quantize_weights_fp8.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          _P, _P, _P]
+_lib.moe_get_device_error.restype = ctypes.c_int
+_lib.moe_get_device_error.argtypes = [_P]
+
+
+def library():
+    """The loaded ctypes handle of libmoe.so."""
+    return _lib
+
+
+@dataclass
+class LayerCfg:
+    """Shape of one layer (mirror of moe_cfg_t with readable names)."""
+    T: int
+    d: int
+    E: int
+    n_groups: int
+    topk_groups: int
+    k: int
+    n_shared: int
+    inter: int
+    route_scale: float = 1.0
+    gamma: float = 1e-3
+    dtype: str = "bf16"
+    group_score_topn: int = 2
+
+    def c(self) -> MoeCfg:
+        return MoeCfg(self.T, self.d, self.E, self.n_groups, self.topk_groups, self.k,
+                      self.n_shared, self.inter, self.group_score_topn,
+                      float(self.route_scale), float(self.gamma), _DTYPES[self.dtype])
+
+    @classmethod
+    def from_shape(cls, shape, **kw):
+        """From a moe_synth.LayerShape (or anything with the same fields)."""
+        c = cls(shape.T, shape.d, shape.E, shape.n_groups, shape.topk_groups, shape.k,
+                shape.n_shared, shape.inter, shape.route_scale, shape.gamma, shape.dtype,
+                shape.group_score_topn)
+        for k, v in kw.items():
+            setattr(c, k, v)
+        return c
+
+
+def _ptr(t, name, dtype=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be in CUDA device memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise MoeError(fn, status)
+
+
+def _cfg(cfg):
+    return ctypes.byref(cfg.c() if isinstance(cfg, LayerCfg) else cfg)
+
+
+_X = (torch.float32, torch.bfloat16)
+_F8 = (torch.float8_e4m3fn, torch.uint8)
+
+
+def moe_check_cfg(cfg):
+    return _lib.moe_check_cfg(_cfg(cfg))
+
+
+def moe_workspace_bytes(cfg):
+    return int(_lib.moe_workspace_bytes(_cfg(cfg)))
+
+
+def moe_route(cfg, x, router_w, bias, topk_idx, topk_w, counts, offsets, row_of_slot,
+              token_of_row, ws, affinity_in=None, affinity_out=None, stream=None):
+    _check("moe_route", _lib.moe_route(
+        _cfg(cfg), _ptr(x, "x", _X, allow_none=affinity_in is not None),
+        _ptr(router_w, "router_w", torch.float32, allow_none=affinity_in is not None),
+        _ptr(bias, "bias", torch.float32),
+        _ptr(affinity_in, "affinity_in", torch.float32, allow_none=True),
+        _ptr(affinity_out, "affinity_out", torch.float32, allow_none=True),
+        _ptr(topk_idx, "topk_idx", torch.int32), _ptr(topk_w, "topk_w", torch.float32),
+        _ptr(counts, "counts", torch.int32), _ptr(offsets, "offsets", torch.int32),
+        _ptr(row_of_slot, "row_of_slot", torch.int32),
+        _ptr(token_of_row, "token_of_row", torch.int32),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_permute(cfg, x, token_of_row, x_perm, x_perm_scales=None, x_q=None, x_q_scales=None,
+                stream=None):
+    _check("moe_permute", _lib.moe_permute(
+        _cfg(cfg), _ptr(x, "x", _X), _ptr(token_of_row, "token_of_row", torch.int32),
+        _ptr(x_perm, "x_perm", _X + _F8),
+        _ptr(x_perm_scales, "x_perm_scales", torch.float32, allow_none=True),
+        _ptr(x_q, "x_q", _F8, allow_none=True),
+        _ptr(x_q_scales, "x_q_scales", torch.float32, allow_none=True), _stream(stream)))
+
+
+def moe_experts_grouped(cfg, x_perm, x, offsets, w13, w2, ws13, ws2, y_perm, y_shared, ws,
+                        x_perm_scales=None, x_scales=None, w13_scales=None, w2_scales=None,
+                        ws13_scales=None, ws2_scales=None, stream=None):
+    _check("moe_experts_grouped", _lib.moe_experts_grouped(
+        _cfg(cfg), _ptr(x_perm, "x_perm", _X + _F8),
+        _ptr(x_perm_scales, "x_perm_scales", torch.float32, allow_none=True),
+        _ptr(x, "x", _X + _F8, allow_none=True),
+        _ptr(x_scales, "x_scales", torch.float32, allow_none=True),
+        _ptr(offsets, "offsets", torch.int32), _ptr(w13, "w13", _X + _F8),
+        _ptr(w13_scales, "w13_scales", torch.float32, allow_none=True),
+        _ptr(w2, "w2", _X + _F8), _ptr(w2_scales, "w2_scales", torch.float32, allow_none=True),
+        _ptr(ws13, "ws13", _X + _F8, allow_none=True),
+        _ptr(ws13_scales, "ws13_scales", torch.float32, allow_none=True),
+        _ptr(ws2, "ws2", _X + _F8, allow_none=True),
+        _ptr(ws2_scales, "ws2_scales", torch.float32, allow_none=True),
+        _ptr(y_perm, "y_perm", _X), _ptr(y_shared, "y_shared", _X, allow_none=True),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_combine(cfg, y_perm, y_shared, row_of_slot, topk_w, out, stream=None):
+    _check("moe_combine", _lib.moe_combine(
+        _cfg(cfg), _ptr(y_perm, "y_perm", _X), _ptr(y_shared, "y_shared", _X, allow_none=True),
+        _ptr(row_of_slot, "row_of_slot", torch.int32), _ptr(topk_w, "topk_w", torch.float32),
+        _ptr(out, "out", _X), _stream(stream)))
+
+
+def moe_bias_update(cfg, counts, bias, stream=None):
+    _check("moe_bias_update", _lib.moe_bias_update(
+        _cfg(cfg), _ptr(counts, "counts", torch.int32), _ptr(bias, "bias", torch.float32),
+        _stream(stream)))
+
+
+def moe_quantize_weights_fp8(w, q, scales, stream=None):
+    """w [n, rows, cols] bf16 -> q [n, rows, cols] E4M3, scales [n, rows/128, cols/128]."""
+    w3 = w if w.dim() == 3 else w.unsqueeze(0)
+    _check("moe_quantize_weights_fp8", _lib.moe_quantize_weights_fp8(
+        _ptr(w, "w", torch.bfloat16), w3.shape[0], w3.shape[1], w3.shape[2],
+        _ptr(q, "q", _F8), _ptr(scales, "scales", torch.float32), _stream(stream)))
+
+
+def moe_get_device_error(stream=None):
+    """Synchronises the stream and returns (and clears) the device error status."""
+    return _lib.moe_get_device_error(_stream(stream))
+
+
+from .layer import MoELayer  # noqa: E402,F401

@@ -1,0 +1,446 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// fed by TMA, for the bf16 kind.
+//
+// "DeepSeek-V3 Technical Report", DeepSeekMoE paragraph: each routed expert
+// is an FFN applied to the tokens routed to it, and the shared experts to
+// every token.  Each FFN is SwiGLU: h = silu(u W1^T) * (u W3^T), y = h W2^T.
+//
+// Two launches per layer, one persistent kernel each:
+//   gate/up: [a | b] = A W13^T per 128 x 256 tile, h = silu(a) * b in the
+//            epilogue (the tile's 256 MMA columns are 128 gate rows and the
+//            128 matching up rows of W13, so a tile yields 128 h columns);
+//   down:    y = h W2^T per 128 x 256 tile.
+// The work list is every (group, M tile, N tile) of the routed experts
+// (segment sizes read from `offsets` in device memory) followed by the
+// shared class (all T rows, intermediate N_s * I).  CTA i takes tiles
+// i, i + grid, ...; inside a group the M tile varies fastest, so the CTAs
+// running at the same time share each weight tile through L2.
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: A and B tiles into a 4-stage shared-memory ring
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, N=256,
+//               K=16) into one of two 256-column fp32 accumulators
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM
+//               lanes 32*(w%4) .. +31), SwiGLU or copy, bf16 stores with
+//               the segment's tail rows masked
+// Every wait is bounded (see mbar_wait); a wait that gives up sets the
+// error word and a block-wide abort flag so that all roles leave, drain
+// their own copies in flight and free TMEM.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace bf16gemm {
+
+constexpr int BM = 128, BN = 256, BK = 64;  // BK * 2 bytes = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KiB
+constexpr int B_HALF_BYTES = B_BYTES / 2;    // one 128-row box
+constexpr int THREADS = 192;
+constexpr int MAX_GROUPS = 1025;             // 1024 routed experts + the shared class
+constexpr uint32_t TMEM_COLS = 512;          // two 256-column accumulators
+constexpr uint32_t IDESC = idesc_f32acc(1, 1, BM, BN);
+
+enum { GATEUP = 0, DOWN = 1 };
+
+struct ClassDesc {
+  __nv_bfloat16* out;  // output rows of the class
+  int ld_out;          // output row stride, elements
+  int n_out;           // output columns (h columns for gate/up, d for down)
+  int k_dim;           // reduction length
+};
+
+struct Params {
+  CUtensorMap a_map[2];  // [0] routed rows, [1] shared rows
+  CUtensorMap b_map[2];  // [0] routed weights, [1] shared weights
+  ClassDesc cls[2];
+  const int32_t* offsets;
+  int E;
+  int T;
+  int has_shared;
+  int inter;  // I: intermediate size of one expert
+  int d;
+};
+
+struct Smem {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+  int n_groups;
+  int gstart[MAX_GROUPS + 1];  // first tile of every group
+  int mtiles[MAX_GROUPS];      // M tiles of every group
+};
+
+constexpr size_t kRingBytes = static_cast<size_t>(STAGES) * (A_BYTES + B_BYTES);
+constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(Smem);
+
+struct Tile {
+  int cls;      // 0 routed, 1 shared
+  int group;    // routed expert index (cls 0)
+  int row0;     // first row of the group in its class's row space
+  int rows;     // valid rows of the group
+  int mt, nt;   // tile coordinates inside the group
+};
+
+template <int MODE>
+__device__ __forceinline__ int out_tile_cols() { return MODE == GATEUP ? BN / 2 : BN; }
+
+template <int MODE>
+__device__ __forceinline__ int n_tiles_of(const Params& p, int cls) {
+  return ceil_div(p.cls[cls].n_out, out_tile_cols<MODE>());
+}
+
+// Warp-cooperative build of the tile table from the segment offsets.
+template <int MODE>
+__device__ void build_tile_table(const Params& p, Smem& s) {
+  const int lane = threadIdx.x % 32;
+  const int G = p.E + (p.has_shared ? 1 : 0);
+  const int per = ceil_div(G, 32);
+  const int g0 = lane * per, g1 = min(G, g0 + per);
+  int sum = 0;
+  for (int g = g0; g < g1; ++g) {
+    int rows, cls;
+    if (g < p.E) { rows = p.offsets[g + 1] - p.offsets[g]; cls = 0; }
+    else { rows = p.T; cls = 1; }
+    const int mt = ceil_div(max(rows, 0), BM);
+    s.mtiles[g] = mt;
+    sum += mt * n_tiles_of<MODE>(p, cls);
+  }
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int run = incl - sum;
+  for (int g = g0; g < g1; ++g) {
+    s.gstart[g] = run;
+    const int cls = g < p.E ? 0 : 1;
+    run += s.mtiles[g] * n_tiles_of<MODE>(p, cls);
+  }
+  if (lane == 31) { s.gstart[G] = incl; s.n_groups = G; }
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int t) {
+  int lo = 0, hi = s.n_groups;  // gstart[lo] <= t < gstart[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s.gstart[mid] <= t) lo = mid; else hi = mid;
+  }
+  Tile tl;
+  tl.cls = lo < p.E ? 0 : 1;
+  tl.group = lo;
+  const int local = t - s.gstart[lo];
+  const int mt_count = s.mtiles[lo];
+  tl.mt = local % mt_count;
+  tl.nt = local / mt_count;
+  if (tl.cls == 0) { tl.row0 = p.offsets[lo]; tl.rows = p.offsets[lo + 1] - tl.row0; }
+  else { tl.row0 = 0; tl.rows = p.T; }
+  return tl;
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+  int never = 0;
+  return mbar_wait(bar, parity, &never);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1) experts_bf16_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Smem& s = *reinterpret_cast<Smem*>(ring + kRingBytes);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  volatile int* abort_flag = &s.abort;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) { tma_prefetch_desc(&p.a_map[i]); tma_prefetch_desc(&p.b_map[i]); }
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&s.tfull[i], 1); mbar_init(&s.tempty[i], 4); }
+    mbar_init(&s.done, 1);
+    s.abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (warp == 2) build_tile_table<MODE>(p, s);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s.tmem_base;
+  const int total = s.gstart[s.n_groups];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_a = l2_policy_evict_last();
+      const uint64_t pol_b = l2_policy_evict_normal();
+      uint32_t stage = 0, phase = 0;
+      int issued = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const Tile tl = decode_tile<MODE>(p, s, t);
+        const ClassDesc& cd = p.cls[tl.cls];
+        const int nk = cd.k_dim / BK;
+        const int a_row = tl.row0 + tl.mt * BM;
+        const CUtensorMap* am = &p.a_map[tl.cls];
+        const CUtensorMap* bm = &p.b_map[tl.cls];
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) break;
+          uint8_t* sa = ring + stage * A_BYTES;
+          uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
+          mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
+          tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
+          int bx, by0, by1;
+          if (MODE == GATEUP) {
+            // 128 h columns starting at n0: W1 rows and the matching W3 rows
+            const int n0 = tl.nt * (BN / 2);
+            const int sh = n0 / p.inter, i0 = n0 % p.inter;
+            const int base = (tl.cls == 0 ? tl.group : sh) * 2 * p.inter;
+            bx = kb * BK;
+            by0 = base + i0;
+            by1 = base + p.inter + i0;
+          } else {
+            // 256 output columns of d; K block kb of expert-local index
+            const int k0 = kb * BK;
+            const int sh = k0 / p.inter;
+            const int ex = tl.cls == 0 ? tl.group : sh;
+            bx = tl.cls == 0 ? k0 : k0 % p.inter;
+            by0 = ex * p.d + tl.nt * BN;
+            by1 = by0 + BN / 2;
+          }
+          tma_load_2d(sb, bm, &s.full[stage], bx, by0, pol_b);
+          tma_load_2d(sb + B_HALF_BYTES, bm, &s.full[stage], bx, by1, pol_b);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Drain: wait until the last loads of every stage have landed.
+      for (int i = 0; i < STAGES && i < issued; ++i) {
+        if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+        drain_wait(&s.full[stage], phase);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      bool any = false;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++it) {
+        const Tile tl = decode_tile<MODE>(p, s, t);
+        const int nk = p.cls[tl.cls].k_dim / BK;
+        const int acc = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!mbar_wait(&s.tempty[acc], use ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&s.full[stage], phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(ring + stage * A_BYTES);
+          const uint32_t b0 = smem_u32(ring + STAGES * A_BYTES + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32),
+                        IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
+          any = true;
+          mma_commit(&s.empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&s.tfull[acc]);
+      }
+      // Drain: every MMA issued by this thread has completed after this.
+      if (any) {
+        mma_commit(&s.done);
+        drain_wait(&s.done, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const Tile tl = decode_tile<MODE>(p, s, t);
+      const ClassDesc& cd = p.cls[tl.cls];
+      const int acc = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+      if (!mbar_wait(&s.tfull[acc], use, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+      const int m = tl.mt * BM + r_in_tile;
+      const bool valid = m < tl.rows;
+      const int n_base = tl.nt * out_tile_cols<MODE>();
+      __nv_bfloat16* orow = cd.out + static_cast<size_t>(tl.row0 + (valid ? m : 0)) * cd.ld_out + n_base;
+      if (MODE == GATEUP) {
+#pragma unroll 1
+        for (int c = 0; c < (BN / 2) / 16; ++c) {
+          float a[16], b[16];
+          tmem_ld16(taddr + c * 16, a);
+          tmem_ld16(taddr + BN / 2 + c * 16, b);
+          tmem_ld_wait();
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            pk[i] = pack_bf16x2(silu_f(a[2 * i]) * b[2 * i], silu_f(a[2 * i + 1]) * b[2 * i + 1]);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16];
+          tmem_ld16(taddr + c * 16, v);
+          tmem_ld_wait();
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          if (valid && n_base + c * 16 < cd.n_out) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.tempty[acc]);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace bf16gemm
+
+// ------------------------------------------------------------------- host
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+size_t experts_scratch_bytes(const moe_cfg_t& c) {
+  const size_t tk = static_cast<size_t>(c.T) * c.K;
+  const size_t hr = tk * c.inter, hs = static_cast<size_t>(c.T) * c.n_shared * c.inter;
+  if (c.dtype == MOE_DTYPE_FP32) return align_up((hr + hs) * 4, 256);
+  if (c.dtype == MOE_DTYPE_BF16) return align_up((hr + hs) * 2, 256);
+  // FP8: E4M3 codes plus one fp32 scale per 128 values
+  return align_up(hr + hs, 256) + align_up((hr + hs) / 128 * 4, 256);
+}
+
+void experts_scratch_carve(const moe_cfg_t& c, void* ws, void** h, float** h_scales) {
+  const size_t tk = static_cast<size_t>(c.T) * c.K;
+  const size_t hr = tk * c.inter, hs = static_cast<size_t>(c.T) * c.n_shared * c.inter;
+  *h = ws;
+  *h_scales = nullptr;
+  if (c.dtype == MOE_DTYPE_FP8_E4M3)
+    *h_scales = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(hr + hs, 256));
+}
+
+template <int MODE>
+static cudaError_t launch_bf16_gemm(const bf16gemm::Params& prm, cudaStream_t st) {
+  using namespace bf16gemm;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(experts_bf16_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  experts_bf16_kernel<MODE><<<sm_count(), THREADS, kSmemBytes, st>>>(prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
+  using namespace bf16gemm;
+  const moe_cfg_t& c = *a.cfg;
+  const int64_t tk = static_cast<int64_t>(c.T) * c.K;
+  const int I = c.inter, Ns = c.n_shared;
+  __nv_bfloat16* h_routed = static_cast<__nv_bfloat16*>(a.h);
+  __nv_bfloat16* h_shared = h_routed + tk * I;
+  const bool has_shared = Ns > 0;
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
+
+  // ---- gate/up: A = x_perm / x, B = W13
+  Params g{};
+  g.offsets = a.offsets; g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
+  g.inter = I; g.d = c.d;
+  CUresult r = encode_tensor_map_2d(&g.a_map[0], BF, const_cast<void*>(a.x_perm), c.d, tk,
+                                    static_cast<uint64_t>(c.d) * 2, BK, BM, SW);
+  if (r == CUDA_SUCCESS)
+    r = encode_tensor_map_2d(&g.b_map[0], BF, const_cast<void*>(a.w13), c.d,
+                             static_cast<uint64_t>(c.E) * 2 * I, static_cast<uint64_t>(c.d) * 2,
+                             BK, BN / 2, SW);
+  if (r == CUDA_SUCCESS && has_shared) {
+    r = encode_tensor_map_2d(&g.a_map[1], BF, const_cast<void*>(a.x), c.d, c.T,
+                             static_cast<uint64_t>(c.d) * 2, BK, BM, SW);
+    if (r == CUDA_SUCCESS)
+      r = encode_tensor_map_2d(&g.b_map[1], BF, const_cast<void*>(a.ws13), c.d,
+                               static_cast<uint64_t>(Ns) * 2 * I, static_cast<uint64_t>(c.d) * 2,
+                               BK, BN / 2, SW);
+  } else {
+    g.a_map[1] = g.a_map[0];
+    g.b_map[1] = g.b_map[0];
+  }
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  g.cls[0] = ClassDesc{h_routed, I, I, c.d};
+  g.cls[1] = ClassDesc{h_shared, Ns * I, Ns * I, c.d};
+  cudaError_t e = launch_bf16_gemm<GATEUP>(g, st);
+  if (e != cudaSuccess) return e;
+
+  // ---- down: A = h, B = W2
+  Params dn = g;
+  r = encode_tensor_map_2d(&dn.a_map[0], BF, h_routed, I, tk, static_cast<uint64_t>(I) * 2, BK, BM,
+                           SW);
+  if (r == CUDA_SUCCESS)
+    r = encode_tensor_map_2d(&dn.b_map[0], BF, const_cast<void*>(a.w2), I,
+                             static_cast<uint64_t>(c.E) * c.d, static_cast<uint64_t>(I) * 2, BK,
+                             BN / 2, SW);
+  if (r == CUDA_SUCCESS && has_shared) {
+    r = encode_tensor_map_2d(&dn.a_map[1], BF, h_shared, static_cast<uint64_t>(Ns) * I, c.T,
+                             static_cast<uint64_t>(Ns) * I * 2, BK, BM, SW);
+    if (r == CUDA_SUCCESS)
+      r = encode_tensor_map_2d(&dn.b_map[1], BF, const_cast<void*>(a.ws2), I,
+                               static_cast<uint64_t>(Ns) * c.d, static_cast<uint64_t>(I) * 2, BK,
+                               BN / 2, SW);
+  } else {
+    dn.a_map[1] = dn.a_map[0];
+    dn.b_map[1] = dn.b_map[0];
+  }
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  dn.cls[0] = ClassDesc{static_cast<__nv_bfloat16*>(a.y_perm), c.d, c.d, I};
+  dn.cls[1] = ClassDesc{static_cast<__nv_bfloat16*>(a.y_shared), c.d, c.d, Ns * I};
+  return launch_bf16_gemm<DOWN>(dn, st);
+}
+
+}  // namespace moe

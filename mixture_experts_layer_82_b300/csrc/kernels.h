@@ -1,0 +1,89 @@
+// Host-side launchers of the libmoe kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Tokens per routing tile: the unit of the per-expert histogram and of the
+// within-segment rank (one 32-bit mask per expert and tile).
+constexpr int kRouteTile = 32;
+
+struct RouteScratch {
+  float* affinity;        // [T, E] when the caller keeps none
+  int32_t* tile_counts;   // [ceil(T/32), E], later the per-tile segment base
+};
+
+// Layout of the routing scratch inside a workspace buffer.
+size_t route_scratch_bytes(const moe_cfg_t& c, bool need_affinity);
+RouteScratch route_scratch_carve(const moe_cfg_t& c, void* ws, bool need_affinity);
+
+cudaError_t launch_router_affinity(const moe_cfg_t& c, const void* x, const float* w,
+                                   float* affinity, cudaStream_t s);
+cudaError_t launch_route_select(const moe_cfg_t& c, const float* affinity, const float* bias,
+                                int32_t* topk_idx, float* topk_w, int32_t* local_rank,
+                                int32_t* tile_counts, cudaStream_t s);
+cudaError_t launch_route_scan(const moe_cfg_t& c, int32_t* tile_counts, int32_t* counts,
+                              int32_t* offsets, cudaStream_t s);
+cudaError_t launch_route_assign(const moe_cfg_t& c, const int32_t* topk_idx,
+                                const int32_t* offsets, const int32_t* tile_base,
+                                int32_t* row_of_slot /* in: local rank, out: row */,
+                                int32_t* token_of_row, cudaStream_t s);
+cudaError_t launch_bias_update(const moe_cfg_t& c, const int32_t* counts, float* bias,
+                               cudaStream_t s);
+
+// permute / combine / quantise
+cudaError_t launch_permute(const moe_cfg_t& c, const void* x, const int32_t* token_of_row,
+                           void* x_perm, size_t elem_bytes, cudaStream_t s);
+cudaError_t launch_quantize_act_fp8(const void* x_bf16, int rows, int cols, void* q,
+                                    float* scales, cudaStream_t s);
+cudaError_t launch_permute_fp8(const moe_cfg_t& c, const void* x_q, const float* x_scales,
+                               const int32_t* token_of_row, void* x_perm, float* x_perm_scales,
+                               cudaStream_t s);
+cudaError_t launch_combine(const moe_cfg_t& c, const void* y_perm, const void* y_shared,
+                           const int32_t* row_of_slot, const float* topk_w, void* out,
+                           cudaStream_t s);
+cudaError_t launch_quantize_weights_fp8(const void* w, int n_mats, int rows, int cols, void* q,
+                                        float* scales, cudaStream_t s);
+
+// expert GEMMs
+struct ExpertsArgs {
+  const moe_cfg_t* cfg;
+  const void* x_perm;
+  const float* x_perm_scales;
+  const void* x;
+  const float* x_scales;
+  const int32_t* offsets;
+  const void* w13;
+  const float* w13_scales;
+  const void* w2;
+  const float* w2_scales;
+  const void* ws13;
+  const float* ws13_scales;
+  const void* ws2;
+  const float* ws2_scales;
+  void* y_perm;
+  void* y_shared;
+  void* h;            // workspace: routed rows [T*K, I] then shared rows [T, Ns*I]
+  float* h_scales;    // FP8: [T*K, I/128] then [T, Ns*I/128]
+};
+
+size_t experts_scratch_bytes(const moe_cfg_t& c);
+void experts_scratch_carve(const moe_cfg_t& c, void* ws, void** h, float** h_scales);
+
+cudaError_t launch_experts_fp32(const ExpertsArgs& a, cudaStream_t s);
+cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t s);
+cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t s);
+
+// Driver entry point of cuTensorMapEncodeTiled (resolved once).
+CUresult encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, void* base,
+                              uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                              uint32_t box_inner, uint32_t box_outer,
+                              CUtensorMapSwizzle swizzle);
+
+}  // namespace moe

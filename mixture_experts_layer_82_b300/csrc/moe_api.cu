@@ -1,0 +1,227 @@
+// The C ABI of libmoe (declared in include/moe.h): host-side argument
+// checks, workspace layout and kernel dispatch.  Nothing here allocates
+// device memory; the only library state is the per-device error word.
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int32_t kVersion = 100;  // 0.1.0
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_str(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported shape";
+    case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE: return "device-side check failed";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+int32_t moe_version(void) { return kVersion; }
+
+moe_status_t moe_check_cfg(const moe_cfg_t* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->d < 1 || c->E < 1 || c->K < 1 || c->inter < 1 || c->n_shared < 0 ||
+      c->n_groups < 1 || c->topk_groups < 1 || c->group_score_topn < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_DTYPE_FP32 && c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP8_E4M3)
+    return MOE_ERR_INVALID_ARG;
+  if (c->E % c->n_groups != 0 || c->topk_groups > c->n_groups || c->K > c->E)
+    return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(c->topk_groups) * (c->E / c->n_groups) < c->K) return MOE_ERR_INVALID_ARG;
+  if (!(c->route_scale == c->route_scale) || !(c->gamma == c->gamma)) return MOE_ERR_INVALID_ARG;
+  if (c->T > (1 << 22) || c->E > 1024 || c->K > 32 || c->n_groups > 32 || c->group_score_topn > 8)
+    return MOE_ERR_SHAPE;
+  const int64_t tk = static_cast<int64_t>(c->T) * c->K;
+  if (tk >= (int64_t{1} << 31)) return MOE_ERR_SHAPE;
+  if (c->dtype == MOE_DTYPE_FP32) {
+    if (c->d % 4 != 0) return MOE_ERR_SHAPE;
+    const int64_t m_tiles = (tk + 63) / 64 + c->E + (c->T + 63) / 64;
+    if (m_tiles >= 65535) return MOE_ERR_SHAPE;
+  } else {
+    if (c->d % 128 != 0 || c->inter % 128 != 0) return MOE_ERR_SHAPE;
+    if (c->dtype == MOE_DTYPE_FP8_E4M3) return MOE_ERR_SHAPE;  // kernel not built yet
+  }
+  return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_cfg_t* c) {
+  if (moe_check_cfg(c) != MOE_OK) return 0;
+  const size_t r = route_scratch_bytes(*c, true);
+  const size_t e = experts_scratch_bytes(*c);
+  return r > e ? r : e;
+}
+
+moe_status_t moe_route(const moe_cfg_t* cfg, const void* x, const float* router_w,
+                       const float* bias, const float* affinity_in, float* affinity_out,
+                       int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                       int32_t* row_of_slot, int32_t* token_of_row, void* ws, size_t ws_bytes,
+                       void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (bias == nullptr || topk_idx == nullptr || topk_w == nullptr || counts == nullptr ||
+      offsets == nullptr || row_of_slot == nullptr || token_of_row == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (affinity_in == nullptr && (x == nullptr || router_w == nullptr)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, router_w, bias, affinity_in, affinity_out, topk_idx, topk_w,
+                        counts, offsets, row_of_slot, token_of_row, ws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  const bool need_aff = affinity_in == nullptr && affinity_out == nullptr;
+  if (ws_bytes < route_scratch_bytes(c, need_aff)) return MOE_ERR_WORKSPACE;
+  const RouteScratch rs = route_scratch_carve(c, ws, need_aff);
+  cudaStream_t s = as_stream(stream);
+  const float* aff = affinity_in;
+  if (aff == nullptr) {
+    float* dst = affinity_out != nullptr ? affinity_out : rs.affinity;
+    cudaError_t e = launch_router_affinity(c, x, router_w, dst, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    aff = dst;
+  } else if (affinity_out != nullptr && affinity_out != affinity_in) {
+    cudaError_t e = cudaMemcpyAsync(affinity_out, affinity_in,
+                                    static_cast<size_t>(c.T) * c.E * sizeof(float),
+                                    cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  cudaError_t e = launch_route_select(c, aff, bias, topk_idx, topk_w, row_of_slot, rs.tile_counts, s);
+  if (e == cudaSuccess) e = launch_route_scan(c, rs.tile_counts, counts, offsets, s);
+  if (e == cudaSuccess)
+    e = launch_route_assign(c, topk_idx, offsets, rs.tile_counts, row_of_slot, token_of_row, s);
+  return from_cuda(e);
+}
+
+moe_status_t moe_permute(const moe_cfg_t* cfg, const void* x, const int32_t* token_of_row,
+                         void* x_perm, float* x_perm_scales, void* x_q, float* x_q_scales,
+                         void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (x == nullptr || token_of_row == nullptr || x_perm == nullptr) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = c.dtype == MOE_DTYPE_FP8_E4M3;
+  if (fp8 && (x_perm_scales == nullptr || x_q == nullptr || x_q_scales == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, token_of_row, x_perm, x_perm_scales, x_q, x_q_scales};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e;
+  if (fp8) {
+    e = launch_quantize_act_fp8(x, c.T, c.d, x_q, x_q_scales, s);
+    if (e == cudaSuccess) e = launch_permute_fp8(c, x_q, x_q_scales, token_of_row, x_perm, x_perm_scales, s);
+  } else {
+    e = launch_permute(c, x, token_of_row, x_perm, c.dtype == MOE_DTYPE_FP32 ? 4 : 2, s);
+  }
+  return from_cuda(e);
+}
+
+moe_status_t moe_experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
+                                 const float* x_perm_scales, const void* x, const float* x_scales,
+                                 const int32_t* offsets, const void* w13, const float* w13_scales,
+                                 const void* w2, const float* w2_scales, const void* ws13,
+                                 const float* ws13_scales, const void* ws2, const float* ws2_scales,
+                                 void* y_perm, void* y_shared, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (x_perm == nullptr || offsets == nullptr || w13 == nullptr || w2 == nullptr ||
+      y_perm == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0 && (x == nullptr || ws13 == nullptr || ws2 == nullptr || y_shared == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const bool fp8 = c.dtype == MOE_DTYPE_FP8_E4M3;
+  if (fp8 && (x_perm_scales == nullptr || w13_scales == nullptr || w2_scales == nullptr ||
+              (c.n_shared > 0 && (x_scales == nullptr || ws13_scales == nullptr ||
+                                  ws2_scales == nullptr))))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_perm, x_perm_scales, x, x_scales, offsets, w13, w13_scales, w2,
+                        w2_scales, ws13, ws13_scales, ws2, ws2_scales, y_perm, y_shared, ws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  if (ws_bytes < experts_scratch_bytes(c)) return MOE_ERR_WORKSPACE;
+  ExpertsArgs a{};
+  a.cfg = &c;
+  a.x_perm = x_perm; a.x_perm_scales = x_perm_scales; a.x = x; a.x_scales = x_scales;
+  a.offsets = offsets;
+  a.w13 = w13; a.w13_scales = w13_scales; a.w2 = w2; a.w2_scales = w2_scales;
+  a.ws13 = ws13; a.ws13_scales = ws13_scales; a.ws2 = ws2; a.ws2_scales = ws2_scales;
+  a.y_perm = y_perm; a.y_shared = c.n_shared > 0 ? y_shared : nullptr;
+  experts_scratch_carve(c, ws, &a.h, &a.h_scales);
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e;
+  switch (c.dtype) {
+    case MOE_DTYPE_FP32: e = launch_experts_fp32(a, s); break;
+    case MOE_DTYPE_BF16: e = launch_experts_bf16(a, s); break;
+    default: e = launch_experts_fp8(a, s); break;
+  }
+  return from_cuda(e);
+}
+
+moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y_perm, const void* y_shared,
+                         const int32_t* row_of_slot, const float* topk_w, void* out, void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (y_perm == nullptr || row_of_slot == nullptr || topk_w == nullptr || out == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {y_perm, y_shared, row_of_slot, topk_w, out};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  return from_cuda(launch_combine(c, y_perm, c.n_shared > 0 ? y_shared : nullptr, row_of_slot,
+                                  topk_w, out, as_stream(stream)));
+}
+
+moe_status_t moe_bias_update(const moe_cfg_t* cfg, const int32_t* counts, float* bias,
+                             void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (counts == nullptr || bias == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(counts) || !aligned16(bias)) return MOE_ERR_ALIGN;
+  return from_cuda(launch_bias_update(*cfg, counts, bias, as_stream(stream)));
+}
+
+moe_status_t moe_quantize_weights_fp8(const void* w_bf16, int32_t n_mats, int32_t rows,
+                                      int32_t cols, void* q, float* scales, void* stream) {
+  if (w_bf16 == nullptr || q == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;
+  if (n_mats < 1 || rows < 1 || cols < 1) return MOE_ERR_INVALID_ARG;
+  if (cols % 128 != 0 || n_mats > 65535 || (rows + 127) / 128 > 65535) return MOE_ERR_SHAPE;
+  if (!aligned16(w_bf16) || !aligned16(q) || !aligned16(scales)) return MOE_ERR_ALIGN;
+  return from_cuda(launch_quantize_weights_fp8(w_bf16, n_mats, rows, cols, q, scales,
+                                               as_stream(stream)));
+}
+
+moe_status_t moe_get_device_error(void* stream) {
+  cudaStream_t s = as_stream(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return MOE_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (word != 0 && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (word != 0) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+"""One DeepSeekMoE layer: the buffers of a batch and the five library calls
+of a forward step (route -> permute -> experts -> combine -> bias update),
+enqueued on one stream with no host synchronisation."""
+
+from __future__ import annotations
+
+import torch
+
+from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_combine,
+               moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes)
+
+
+def _quantize(w, stream=None):
+    n, rows, cols = w.shape
+    q = torch.empty(n, rows, cols, dtype=torch.float8_e4m3fn, device=w.device)
+    s = torch.empty(n, (rows + 127) // 128, cols // 128, dtype=torch.float32, device=w.device)
+    moe_quantize_weights_fp8(w, q, s, stream=stream)
+    return q, s
+
+
+class MoELayer:
+    """Weights and per-batch buffers of one layer on one device.
+
+    ``router_w`` [E, d] fp32, ``bias`` [E] fp32 (updated in place by
+    ``forward`` unless ``update_bias=False``), ``w13`` [E, 2I, d],
+    ``w2`` [E, d, I], ``ws13``/``ws2`` the shared experts; master weights
+    in bf16 (fp32 for the fp32 kind).  For the fp8 kind the expert weights
+    are quantised once here (128 x 128 blocks)."""
+
+    def __init__(self, cfg: LayerCfg, router_w, bias, w13, w2, ws13=None, ws2=None):
+        self.cfg = cfg
+        dev = router_w.device
+        self.router_w, self.bias = router_w, bias
+        T, d, E, K, I, ns = cfg.T, cfg.d, cfg.E, cfg.k, cfg.inter, cfg.n_shared
+        if cfg.dtype == "fp8":
+            self.w13, self.w13_s = _quantize(w13)
+            self.w2, self.w2_s = _quantize(w2)
+            if ns:
+                self.ws13, self.ws13_s = _quantize(ws13)
+                self.ws2, self.ws2_s = _quantize(ws2)
+            else:
+                self.ws13 = self.ws13_s = self.ws2 = self.ws2_s = None
+        else:
+            self.w13, self.w2, self.ws13, self.ws2 = w13, w2, ws13, ws2
+            self.w13_s = self.w2_s = self.ws13_s = self.ws2_s = None
+        act = torch.float32 if cfg.dtype == "fp32" else torch.bfloat16
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.topk_idx = torch.empty(T, K, **i32)
+        self.topk_w = torch.empty(T, K, dtype=torch.float32, device=dev)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.row_of_slot = torch.empty(T, K, **i32)
+        self.token_of_row = torch.empty(T * K, **i32)
+        if cfg.dtype == "fp8":
+            self.x_perm = torch.empty(T * K, d, dtype=torch.float8_e4m3fn, device=dev)
+            self.x_perm_s = torch.empty(T * K, d // 128, dtype=torch.float32, device=dev)
+            self.x_q = torch.empty(T, d, dtype=torch.float8_e4m3fn, device=dev)
+            self.x_q_s = torch.empty(T, d // 128, dtype=torch.float32, device=dev)
+        else:
+            self.x_perm = torch.empty(T * K, d, dtype=act, device=dev)
+            self.x_perm_s = self.x_q = self.x_q_s = None
+        self.y_perm = torch.empty(T * K, d, dtype=act, device=dev)
+        self.y_shared = torch.empty(T, d, dtype=act, device=dev) if ns else None
+        self.out = torch.empty(T, d, dtype=act, device=dev)
+        self.ws = torch.empty(moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+
+    def forward(self, x, stream=None, update_bias=True, affinity_out=None, affinity_in=None):
+        c = self.cfg
+        moe_route(c, x, self.router_w, self.bias, self.topk_idx, self.topk_w, self.counts,
+                  self.offsets, self.row_of_slot, self.token_of_row, self.ws,
+                  affinity_in=affinity_in, affinity_out=affinity_out, stream=stream)
+        moe_permute(c, x, self.token_of_row, self.x_perm, self.x_perm_s, self.x_q, self.x_q_s,
+                    stream=stream)
+        shared_in = self.x_q if c.dtype == "fp8" else x
+        moe_experts_grouped(c, self.x_perm, shared_in, self.offsets, self.w13, self.w2,
+                            self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
+                            x_perm_scales=self.x_perm_s, x_scales=self.x_q_s,
+                            w13_scales=self.w13_s, w2_scales=self.w2_s,
+                            ws13_scales=self.ws13_s, ws2_scales=self.ws2_s, stream=stream)
+        moe_combine(c, self.y_perm, self.y_shared, self.row_of_slot, self.topk_w, self.out,
+                    stream=stream)
+        if update_bias:
+            moe_bias_update(c, self.counts, self.bias, stream=stream)
+        return self.out

@@ -1,0 +1,142 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and its host-side argument checks answer before any launch."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_82_b300 as moe
+from moe_synth import CONFIGS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert "moe_route" in names and "moe_experts_grouped" in names
+    lib = moe.library()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moe.EXPORTED)
+
+
+def _param_counts():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(moe_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_header():
+    lib = moe.library()
+    counts = _param_counts()
+    assert set(counts) == set(moe.EXPORTED)
+    for name, n in counts.items():
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None and len(argtypes) == n, (name, n, argtypes)
+
+
+def test_cfg_struct_layout():
+    # 9 int32 + 2 float + 1 int32, no padding
+    assert ctypes.sizeof(moe.MoeCfg) == 48
+    assert moe.MoeCfg.route_scale.offset == 36 and moe.MoeCfg.dtype.offset == 44
+
+
+def test_version_and_status_strings():
+    lib = moe.library()
+    assert lib.moe_version() >= 100
+    for code in range(8):
+        assert lib.moe_status_str(code).decode()
+    assert lib.moe_status_str(99).decode() == "unknown status"
+
+
+@pytest.mark.parametrize("name", sorted(CONFIGS))
+def test_workloads_pass_the_checks(name):
+    cfg = moe.LayerCfg.from_shape(CONFIGS[name])
+    if cfg.dtype == "fp8" and moe.moe_check_cfg(cfg) == 2:
+        pytest.skip("fp8 kind not enabled")
+    assert moe.moe_check_cfg(cfg) == 0
+    assert moe.moe_workspace_bytes(cfg) > 0
+
+
+def _base(**kw):
+    c = moe.LayerCfg.from_shape(CONFIGS["mid_bf16"])
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), 1), (dict(E=63), 1), (dict(topk_groups=9), 1), (dict(k=65), 1),
+    (dict(n_groups=64, topk_groups=1, k=2), 1),   # kept groups hold fewer than K experts
+    (dict(d=2000), 2), (dict(inter=1400), 2), (dict(T=(1 << 22) + 1), 2),
+    (dict(group_score_topn=0), 1), (dict(group_score_topn=9), 2), (dict(n_shared=-1), 1),
+    (dict(E=2048, n_groups=32), 2), (dict(k=33, E=128), 2), (dict(route_scale=float("nan")), 1),
+])
+def test_bad_configs_are_rejected(kw, status):
+    assert moe.moe_check_cfg(_base(**kw)) == status
+    assert moe.moe_workspace_bytes(_base(**kw)) == 0
+
+
+def test_fp32_kind_allows_any_multiple_of_four():
+    c = _base(dtype="fp32", d=260, inter=100)
+    assert moe.moe_check_cfg(c) == 0
+    assert moe.moe_check_cfg(_base(dtype="fp32", d=258)) == 2
+
+
+def _route_raw(cfg, ptrs, ws_bytes=1 << 20):
+    lib = moe.library()
+    return lib.moe_route(ctypes.byref(cfg.c()), *ptrs, ws_bytes, None)
+
+
+def test_route_rejects_null_and_misaligned_pointers_without_launching():
+    cfg = _base()
+    good = [0x10000 * (i + 1) for i in range(12)]  # never dereferenced: checks come first
+    ptrs = list(good)
+    ptrs[2] = None  # bias
+    assert _route_raw(cfg, ptrs) == 1
+    ptrs = list(good)
+    ptrs[3] = None; ptrs[0] = None  # neither x nor affinity_in
+    assert _route_raw(cfg, ptrs) == 1
+    ptrs = list(good)
+    ptrs[5] += 4  # topk_idx misaligned
+    assert _route_raw(cfg, ptrs) == 3
+    assert _route_raw(cfg, good, ws_bytes=16) == 7  # workspace too small
+
+
+def test_other_calls_check_before_launching():
+    lib = moe.library()
+    cfg = ctypes.byref(_base().c())
+    a = 0x100000
+    assert lib.moe_permute(cfg, None, a, a, None, None, None, None) == 1
+    assert lib.moe_combine(cfg, a, a, a + 8, a, a, None) == 3
+    assert lib.moe_bias_update(cfg, None, a, None) == 1
+    assert lib.moe_quantize_weights_fp8(a, 1, 128, 100, a, a, None) == 2
+    assert lib.moe_quantize_weights_fp8(a, 0, 128, 128, a, a, None) == 1
+    args = [None] * 15
+    assert lib.moe_experts_grouped(cfg, *args, None, 0, None) == 1
+    fp8 = _base(dtype="fp8")
+    if moe.moe_check_cfg(fp8) == 0:
+        # FP8 without scale pointers
+        p = [a] * 15
+        p[1] = None
+        assert lib.moe_experts_grouped(ctypes.byref(fp8.c()), *p, a, 1 << 40, None) == 1
+
+
+def test_binding_refuses_host_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        moe.moe_bias_update(_base(), torch.zeros(64, dtype=torch.int32),
+                            torch.zeros(64, dtype=torch.float32), stream=0)
