@@ -1,0 +1,388 @@
+"""Benchmark of the DeepSeekMoE layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload v3_bf16|v3_fp8|v3_decode|mid_bf16]
+
+A step is one pass of the whole layer (route -> permute -> grouped expert
+GEMMs -> combine -> bias update) over one batch of T tokens, with every
+input already resident in device memory.  The default workload is the
+DeepSeek-V3-shaped layer in bf16 (T=8192, d=7168, 256 routed experts in 8
+groups, top-4 groups, top-8, 1 shared expert, I=2048, route scale 2.5, Zipf
+-skewed router).  With N > 1 (torchrun) every rank runs its own replica on
+its own batch (weak scaling, no collective on the data path); the time is
+the maximum over ranks.  Rank 0 prints one JSON line.
+
+``--impl reference`` times the CPU oracle (fp64 NumPy) on the host cores on a
+bounded sample of the same workload; that is the only other place, besides
+the ``cpu_baseline`` leg, where this script runs the oracle.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_synth import CONFIGS, make_layer  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at V3 shape (bf16, FP8); TFLOP/s as % of B300 peak"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+KERNEL_SRC = {"bf16": "mixture_experts_layer_82_b300/csrc/experts_sm100.cu",
+              "fp8": "mixture_experts_layer_82_b300/csrc/experts_fp8.cu"}
+
+
+# --------------------------------------------------------------- workload
+
+def describe(shape):
+    return (f"{shape.name}: T={shape.T}, d={shape.d}, E={shape.E} routed in {shape.n_groups} "
+            f"groups (top-{shape.topk_groups} groups), top-{shape.k}, {shape.n_shared} shared, "
+            f"I={shape.inter}, route scale {shape.route_scale}, {shape.dtype}, router "
+            f"{shape.router}, seed {shape.seed}")
+
+
+def expert_flops(shape):
+    """Algorithmic FLOPs of the expert GEMMs: 3 projections of d x I per
+    routed slot and per token for every shared expert (no padding)."""
+    return 6.0 * shape.d * shape.inter * (shape.T * shape.k + shape.T * shape.n_shared)
+
+
+def layer_flops(shape):
+    return expert_flops(shape) + 2.0 * shape.T * shape.d * shape.E
+
+
+def launches_per_step(dtype):
+    # route: affinity, select, scan, assign; permute (+ quantise for fp8);
+    # experts: gate/up and down; combine; bias update
+    return {"fp32": 4 + 1 + 2 + 1 + 1, "bf16": 4 + 1 + 2 + 1 + 1, "fp8": 4 + 2 + 2 + 1 + 1}[dtype]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    d = dict(PEAKS_FALLBACK)
+    d["_source"] = "fallback"
+    return d
+
+
+def kernel_traffic(dtype, workload):
+    """DRAM bytes per launch of the expert GEMM pair from the committed ncu
+    summary, if the kernel source has not changed since it was taken."""
+    src = os.path.join(ROOT, KERNEL_SRC.get(dtype, ""))
+    summ = os.path.join(ROOT, "profiles", f"experts_{dtype}_{workload}_traffic.json")
+    if not (os.path.exists(src) and os.path.exists(summ)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    with open(summ) as f:
+        d = json.load(f)
+    if d.get("kernel_src_sha256") != sha:
+        return None
+    return d.get("traffic_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        # "under load": samples drawing more than half of the maximum power seen
+        loaded = [s for s, p in zip(sm, pw) if pw and p > 0.5 * max(pw)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------- CPU baseline
+
+def oracle_sample(shape, L, n_tokens, token0=0):
+    """Runs the fp64 oracle end to end (affinity, selection, gates, experts,
+    combine) on n_tokens tokens of the workload; returns (seconds, tokens).
+    Expert weights are fetched from device memory one expert at a time."""
+    import oracle
+    from oracle import moe_fp8
+
+    class View:
+        def __init__(self, t):
+            self.t = t
+
+        def __len__(self):
+            return self.t.shape[0]
+
+        def __getitem__(self, e):
+            return self.t[e].float().cpu().numpy()
+
+    rows = torch.arange(token0, token0 + n_tokens, device=L["x"].device)
+    x = L["x"][rows].float().cpu().numpy()
+    rw = L["router_w"].cpu().numpy()
+    b = L["bias"].cpu().numpy()
+    t0 = time.perf_counter()
+    s = oracle.sigmoid_affinity(x, rw)
+    idx = oracle.select_experts(s.astype(np.float32), b, shape.n_groups, shape.topk_groups,
+                                shape.k, shape.group_score_topn)
+    g = oracle.gating_weights(s, idx, shape.route_scale)
+    fn = moe_fp8.moe_layer_tokens_fp8 if shape.dtype == "fp8" else oracle.moe_layer_tokens
+    fn(x, idx, g, View(L["w13"]), View(L["w2"]), View(L["ws13"]), View(L["ws2"]))
+    return time.perf_counter() - t0, n_tokens
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+# ------------------------------------------------------------------- arms
+
+def run_reference(args, shape, world, rank):
+    """The oracle as it stands, timed on the host cores: each step is a bounded
+    sample of the workload (args.ref_tokens tokens end to end)."""
+    if rank != 0:
+        return 0
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    L = make_layer(shape, dev)
+    for i in range(args.warmup):
+        oracle_sample(shape, L, args.ref_tokens, token0=i * args.ref_tokens)
+    secs, toks = 0.0, 0
+    for i in range(args.steps):
+        s, n = oracle_sample(shape, L, args.ref_tokens,
+                             token0=((args.warmup + i) * args.ref_tokens) % (shape.T - args.ref_tokens))
+        secs += s
+        toks += n
+    value = toks / secs
+    cores = blas_threads()
+    sample = (f"{args.ref_tokens} tokens of the {shape.name} batch per step, end to end "
+              f"(affinity, group-limited top-k, gates, shared + routed SwiGLU experts in fp64, "
+              f"combine); expert weights fetched from device memory per expert")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(shape)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, shape, world, rank, local):
+    import mixture_experts_layer_82_b300 as moe
+
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    L = make_layer(shape, dev)
+    cfg = moe.LayerCfg.from_shape(shape)
+    layer = moe.MoELayer(cfg, L["router_w"], L["bias"].clone(), L["w13"], L["w2"],
+                         L["ws13"] if shape.n_shared else None, L["ws2"] if shape.n_shared else None)
+    x = L["x"]
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        layer.forward(x)
+    torch.cuda.synchronize()
+    status = moe.moe_get_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error status {status} after warm-up")
+
+    # ---- device-resident timing
+    K = args.steps
+    ev_exp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        layer.forward(x, expert_events=ev_exp[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    exp_ms = [a.elapsed_time(b) for a, b in ev_exp]
+    status = moe.moe_get_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error status {status} in the timed region")
+
+    # ---- end to end through host buffers (pinned), copies inside the region
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty(shape.T, shape.d, dtype=layer.out.dtype).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev)
+        out_host.copy_(layer.out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev)
+        out_host.copy_(layer.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+
+    peaks = load_peaks()
+    tokens = world * shape.T * K
+    value = tokens / (total_ms * 1e-3)
+    exp_mean = statistics.mean(exp_ms)
+    achieved = expert_flops(shape) / (exp_mean * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype, "data": "synthetic",
+        "config": {"workload": describe(shape), "global_batch": world * shape.T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: every step streams all expert weights "
+                         f"({(3 * shape.d * shape.inter * (shape.E + shape.n_shared)) * (1 if shape.dtype == 'fp8' else 2) / 1e9:.1f} GB)"},
+        "layer_tflops": layer_flops(shape) * world * K / (total_ms * 1e-3) / 1e12,
+        "roofline": {"bound": "tensor", "kernel": "experts_bf16_kernel (gate/up + down launches "
+                     "of one moe_experts_grouped call)", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_kind": f"bf16 dense burst, {peaks['_source']}",
+                     "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
+                     "traffic": kernel_traffic(shape.dtype, shape.name),
+                     "expert_ms_per_step": exp_mean},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": out_host.numel() * out_host.element_size()},
+        "gpu_launches": launches_per_step(shape.dtype) * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, n = oracle_sample(shape, L, args.cpu_tokens)
+        line["cpu_baseline"] = {
+            "value": n / secs, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} tokens of the same batch end to end through the fp64 oracle "
+                      f"({secs:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="v3_bf16", choices=sorted(CONFIGS))
+    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed steps
+    shape = CONFIGS[args.workload]
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, shape, world, rank)
+        return run_ours(args, shape, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -64,7 +64,11 @@ class MoELayer:
         self.out = torch.empty(T, d, dtype=act, device=dev)
         self.ws = torch.empty(moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
 
-    def forward(self, x, stream=None, update_bias=True, affinity_out=None, affinity_in=None):
+    def forward(self, x, stream=None, update_bias=True, affinity_out=None, affinity_in=None,
+                expert_events=None):
+        """One forward step on ``x`` [T, d].  ``expert_events`` (a pair of
+        torch.cuda.Event) are recorded on ``stream`` around the grouped
+        expert GEMMs, for timing them inside a step."""
         c = self.cfg
         moe_route(c, x, self.router_w, self.bias, self.topk_idx, self.topk_w, self.counts,
                   self.offsets, self.row_of_slot, self.token_of_row, self.ws,
@@ -72,11 +76,15 @@ class MoELayer:
         moe_permute(c, x, self.token_of_row, self.x_perm, self.x_perm_s, self.x_q, self.x_q_s,
                     stream=stream)
         shared_in = self.x_q if c.dtype == "fp8" else x
+        if expert_events is not None:
+            expert_events[0].record(stream)
         moe_experts_grouped(c, self.x_perm, shared_in, self.offsets, self.w13, self.w2,
                             self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
                             x_perm_scales=self.x_perm_s, x_scales=self.x_q_s,
                             w13_scales=self.w13_s, w2_scales=self.w2_s,
                             ws13_scales=self.ws13_s, ws2_scales=self.ws2_s, stream=stream)
+        if expert_events is not None:
+            expert_events[1].record(stream)
         moe_combine(c, self.y_perm, self.y_shared, self.row_of_slot, self.topk_w, self.out,
                     stream=stream)
         if update_bias:
