@@ -1,6 +1,8 @@
 """Build libmoe.so in-tree with nvcc for sm_103a (B300).
 
-    python -m mixture_experts_layer_82_b300.build [--force] [-v]
+    python mixture_experts_layer_82_b300/build.py [--force] [-v]
+
+(run it by path: importing the package needs the library it builds)
 
 The library is one translation unit (csrc/libmoe.cu); it is rebuilt when any
 file under csrc/ or include/ is newer than the shared object.
