@@ -229,6 +229,37 @@ moe_status_t moe_quantize_weights_fp8(const void* w_bf16, int32_t n_mats,
                                       int32_t rows, int32_t cols, void* q,
                                       float* scales, void* stream);
 
+/*
+ * moe_route_static_scratch - moe_route without a workspace argument.
+ *
+ * The paper has no counterpart: this entry point exists for callers that
+ * cannot call cudaMalloc - for example a plugin running inside a serving
+ * engine that has already reserved all device memory for its own pool and
+ * exposes no allocator, or a latency-critical caller that must not pay the
+ * device-wide synchronisation an allocation can cause.  Arguments, outputs
+ * and results are those of moe_route; the caller still passes every input
+ * and output buffer.
+ *
+ * Scratch: a 16 MiB array inside the library, reserved on every GPU that
+ * loads the library until the process exits.  A shape needs
+ *     align256(ceil(T/32) * E * 4)
+ *   + align256(T * E * 4)   only when both affinity_in and affinity_out are NULL
+ * bytes of it; a larger shape is rejected with MOE_ERR_WORKSPACE before
+ * anything is launched.  The call allocates nothing.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  Every call shares the one array and it keeps the last
+ * call's contents (no call needs it cleared): calls that overlap on the GPU
+ * (on different streams, or from several host threads) race on it.
+ */
+moe_status_t moe_route_static_scratch(const moe_cfg_t* cfg, const void* x,
+                                      const float* router_w, const float* bias,
+                                      const float* affinity_in, float* affinity_out,
+                                      int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                      int32_t* offsets, int32_t* row_of_slot,
+                                      int32_t* token_of_row, void* stream);
+
 /* Synchronises `stream`, returns the device error word (MOE_OK if clear,
  * MOE_ERR_TIMEOUT if a wait gave up, MOE_ERR_DEVICE for any other device
  * check) and clears it. */

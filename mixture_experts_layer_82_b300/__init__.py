@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m mixture_experts_layer_82_b300.build`")
+        f"{LIB_PATH} is missing: build it with `python mixture_experts_layer_82_b300/build.py`")
 _lib = ctypes.CDLL(LIB_PATH)
 
 DTYPE_FP32, DTYPE_BF16, DTYPE_FP8_E4M3 = 0, 1, 2
@@ -38,7 +38,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR
 
 EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_bytes",
             "moe_route", "moe_permute", "moe_experts_grouped", "moe_combine",
-            "moe_bias_update", "moe_quantize_weights_fp8", "moe_get_device_error")
+            "moe_bias_update", "moe_quantize_weights_fp8", "moe_get_device_error",
+            "moe_route_static_scratch")
 
 
 class MoeCfg(ctypes.Structure):
@@ -82,6 +83,8 @@ _lib.moe_quantize_weights_fp8.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ct
                                           _P, _P, _P]
 _lib.moe_get_device_error.restype = ctypes.c_int
 _lib.moe_get_device_error.argtypes = [_P]
+_lib.moe_route_static_scratch.restype = ctypes.c_int
+_lib.moe_route_static_scratch.argtypes = [_CFG] + [_P] * 11 + [_P]
 
 
 def library():
@@ -177,6 +180,23 @@ def moe_route(cfg, x, router_w, bias, topk_idx, topk_w, counts, offsets, row_of_
         _ptr(row_of_slot, "row_of_slot", torch.int32),
         _ptr(token_of_row, "token_of_row", torch.int32),
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_route_static_scratch(cfg, x, router_w, bias, topk_idx, topk_w, counts, offsets,
+                             row_of_slot, token_of_row, affinity_in=None, affinity_out=None,
+                             stream=None):
+    """moe_route with the library's own fixed scratch array: no workspace
+    argument and no allocation (see include/moe.h)."""
+    _check("moe_route_static_scratch", _lib.moe_route_static_scratch(
+        _cfg(cfg), _ptr(x, "x", _X, allow_none=affinity_in is not None),
+        _ptr(router_w, "router_w", torch.float32, allow_none=affinity_in is not None),
+        _ptr(bias, "bias", torch.float32),
+        _ptr(affinity_in, "affinity_in", torch.float32, allow_none=True),
+        _ptr(affinity_out, "affinity_out", torch.float32, allow_none=True),
+        _ptr(topk_idx, "topk_idx", torch.int32), _ptr(topk_w, "topk_w", torch.float32),
+        _ptr(counts, "counts", torch.int32), _ptr(offsets, "offsets", torch.int32),
+        _ptr(row_of_slot, "row_of_slot", torch.int32),
+        _ptr(token_of_row, "token_of_row", torch.int32), _stream(stream)))
 
 
 def moe_permute(cfg, x, token_of_row, x_perm, x_perm_scales=None, x_q=None, x_q_scales=None,

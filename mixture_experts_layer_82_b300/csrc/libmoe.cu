@@ -7,3 +7,4 @@
 #include "experts_sm100.cu"
 #include "experts_fp8.cu"
 #include "tma.cu"
+#include "route_static.cu"
