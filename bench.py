@@ -58,6 +58,21 @@ def expert_flops(shape):
     return 6.0 * shape.d * shape.inter * (shape.T * shape.k + shape.T * shape.n_shared)
 
 
+def expert_bytes(shape, counts):
+    """Algorithmic DRAM bytes of one moe_experts_grouped call: the weights of
+    every expert that received a token (read once), the shared experts, and
+    the activations (x_perm and x read, h written and read, y written)."""
+    wb = 1 if shape.dtype == "fp8" else (4 if shape.dtype == "fp32" else 2)
+    ab = 4 if shape.dtype == "fp32" else 2
+    touched = int((np.asarray(counts) > 0).sum())
+    weights = 3 * shape.d * shape.inter * wb * (touched + shape.n_shared)
+    rows = shape.T * shape.k
+    act = (rows * shape.d * (wb if shape.dtype == "fp8" else ab) + shape.T * shape.d * ab
+           + 2 * (rows + shape.T * shape.n_shared) * shape.inter * ab
+           + (rows + shape.T * (1 if shape.n_shared else 0)) * shape.d * ab)
+    return weights + act, touched
+
+
 def layer_flops(shape):
     return expert_flops(shape) + 2.0 * shape.T * shape.d * shape.E
 
@@ -327,6 +342,27 @@ def run_ours(args, shape, world, rank, local):
     exp_mean = statistics.mean(exp_ms)
     achieved = expert_flops(shape) / (exp_mean * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
+    ebytes, touched = expert_bytes(shape, layer.counts.cpu().numpy())
+    hbm_achieved = ebytes / (exp_mean * 1e-3) / 1e9
+    kernel = ("experts_bf16_kernel (gate/up + down launches of one moe_experts_grouped call)"
+              if shape.dtype == "bf16" else "grouped expert GEMM pair")
+    traffic = kernel_traffic(shape.dtype, shape.name)
+    if shape.T * shape.k < 16 * shape.E:  # fewer than 16 rows per expert on average
+        # decode-sized batch: the expert GEMMs stream the touched weights
+        roofline = {"bound": "hbm", "kernel": kernel, "achieved": hbm_achieved,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": hbm_achieved / peaks["hbm_gbs"],
+                    "peak_kind": f"HBM copy bandwidth, {peaks['_source']}",
+                    "algorithmic_bytes": ebytes, "experts_touched": touched,
+                    "traffic": traffic, "expert_ms_per_step": exp_mean}
+    else:
+        roofline = {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_kind": f"bf16 dense burst, {peaks['_source']}",
+                    "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
+                    "hbm_gbs": hbm_achieved, "hbm_frac": hbm_achieved / peaks["hbm_gbs"],
+                    "algorithmic_bytes": ebytes, "traffic": traffic,
+                    "expert_ms_per_step": exp_mean}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -336,13 +372,7 @@ def run_ours(args, shape, world, rank, local):
                    "l2": "inputs larger than L2: every step streams all expert weights "
                          f"({(3 * shape.d * shape.inter * (shape.E + shape.n_shared)) * (1 if shape.dtype == 'fp8' else 2) / 1e9:.1f} GB)"},
         "layer_tflops": layer_flops(shape) * world * K / (total_ms * 1e-3) / 1e12,
-        "roofline": {"bound": "tensor", "kernel": "experts_bf16_kernel (gate/up + down launches "
-                     "of one moe_experts_grouped call)", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_kind": f"bf16 dense burst, {peaks['_source']}",
-                     "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
-                     "traffic": kernel_traffic(shape.dtype, shape.name),
-                     "expert_ms_per_step": exp_mean},
+        "roofline": roofline,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": out_host.numel() * out_host.element_size()},

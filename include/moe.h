@@ -240,12 +240,15 @@ moe_status_t moe_quantize_weights_fp8(const void* w_bf16, int32_t n_mats,
  * and results are those of moe_route; the caller still passes every input
  * and output buffer.
  *
- * Scratch: a 16 MiB array inside the library, reserved on every GPU that
- * loads the library until the process exits.  A shape needs
- *     align256(ceil(T/32) * E * 4)
- *   + align256(T * E * 4)   only when both affinity_in and affinity_out are NULL
- * bytes of it; a larger shape is rejected with MOE_ERR_WORKSPACE before
- * anything is launched.  The call allocates nothing.
+ * Scratch: a 32 MiB array inside the library, reserved on every GPU that
+ * loads the library until the process exits.  A call needs the routing part
+ * of moe_workspace_bytes: align256(ceil(T/32) * E * 4) for the per-tile
+ * loads; align256(T * E * 4) for the affinities when both affinity_in and
+ * affinity_out are NULL; and, for the BF16 and FP8 kinds, align256(E * 3d * 2)
+ * for the centroids split into bf16 terms plus, when T is small, at most
+ * 9.7 MB of split-K partial sums.  (DeepSeek-V3 shape E=256, d=7168, T=8192,
+ * no affinity buffer: 19.7 MiB.)  A larger need is rejected with
+ * MOE_ERR_WORKSPACE before anything is launched.  The call allocates nothing.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call before any

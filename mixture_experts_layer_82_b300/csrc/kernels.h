@@ -17,6 +17,7 @@ constexpr int kRouteTile = 32;
 struct RouteScratch {
   float* affinity;        // [T, E] when the caller keeps none
   int32_t* tile_counts;   // [ceil(T/32), E], later the per-tile segment base
+  void* router;           // bf16 kinds: split centroids and split-K partials
 };
 
 // Layout of the routing scratch inside a workspace buffer.
@@ -24,7 +25,10 @@ size_t route_scratch_bytes(const moe_cfg_t& c, bool need_affinity);
 RouteScratch route_scratch_carve(const moe_cfg_t& c, void* ws, bool need_affinity);
 
 cudaError_t launch_router_affinity(const moe_cfg_t& c, const void* x, const float* w,
-                                   float* affinity, cudaStream_t s);
+                                   float* affinity, const RouteScratch& rs, cudaStream_t s);
+size_t router_tc_scratch_bytes(const moe_cfg_t& c);
+cudaError_t launch_router_tc(const moe_cfg_t& c, const void* x, const float* w, float* affinity,
+                             void* scratch, cudaStream_t s);
 cudaError_t launch_route_select(const moe_cfg_t& c, const float* affinity, const float* bias,
                                 int32_t* topk_idx, float* topk_w, int32_t* local_rank,
                                 int32_t* tile_counts, cudaStream_t s);

@@ -2,6 +2,7 @@
 // kernels that set it live in one module (no relocatable device code).
 #include "moe_api.cu"
 #include "route.cu"
+#include "router_sm100.cu"
 #include "permute.cu"
 #include "experts_fp32.cu"
 #include "experts_sm100.cu"

@@ -95,7 +95,7 @@ moe_status_t moe_route(const moe_cfg_t* cfg, const void* x, const float* router_
   const float* aff = affinity_in;
   if (aff == nullptr) {
     float* dst = affinity_out != nullptr ? affinity_out : rs.affinity;
-    cudaError_t e = launch_router_affinity(c, x, router_w, dst, s);
+    cudaError_t e = launch_router_affinity(c, x, router_w, dst, rs, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     aff = dst;
   } else if (affinity_out != nullptr && affinity_out != affinity_in) {

@@ -207,8 +207,10 @@ struct Vec16<float> {
 };
 
 constexpr int kMaxK = 32;
+constexpr int kCombineVecs = 4;  // 16-byte vectors per lane and work item
 
-// One warp per token; each lane owns 16-byte column chunks.
+// One warp per (token, column chunk of 32 * kCombineVecs vectors): enough
+// independent warps for small T, several loads in flight per lane.
 template <typename TY>
 __global__ void __launch_bounds__(kRowWarps * 32) combine_kernel(
     const TY* __restrict__ y_perm, const TY* __restrict__ y_shared,
@@ -216,33 +218,51 @@ __global__ void __launch_bounds__(kRowWarps * 32) combine_kernel(
     int T, int K, int d, int64_t n_rows) {
   using V = Vec16<TY>;
   constexpr int n = V::n;
+  constexpr int chunk = 32 * n * kCombineVecs;
   const int lane = threadIdx.x % 32;
-  for (int64_t t = blockIdx.x * static_cast<int64_t>(kRowWarps) + threadIdx.x / 32; t < T;
-       t += static_cast<int64_t>(gridDim.x) * kRowWarps) {
-    int64_t rows[kMaxK];
-    float g[kMaxK];
-    bool bad = false;
-    for (int k = 0; k < K; ++k) {
-      rows[k] = row_of_slot[t * K + k];
-      g[k] = topk_w[t * K + k];
-      if (rows[k] < 0 || rows[k] >= n_rows) { bad = true; rows[k] = 0; }
+  const int n_chunks = (d + chunk - 1) / chunk;
+  const int64_t items = static_cast<int64_t>(T) * n_chunks;
+  for (int64_t it = blockIdx.x * static_cast<int64_t>(kRowWarps) + threadIdx.x / 32; it < items;
+       it += static_cast<int64_t>(gridDim.x) * kRowWarps) {
+    const int64_t t = it / n_chunks;
+    const int c0 = static_cast<int>(it % n_chunks) * chunk;
+    // lane k < K holds slot k's row and gate
+    int64_t my_row = 0;
+    float my_g = 0.f;
+    if (lane < K) {
+      my_row = row_of_slot[t * K + lane];
+      my_g = topk_w[t * K + lane];
+      if (my_row < 0 || my_row >= n_rows) { raise_error(kErrIndex); my_row = 0; }
     }
-    if (bad && lane == 0) raise_error(kErrIndex);
-    for (int c = lane * n; c < d; c += 32 * n) {
-      float acc[n];
-      if (y_shared != nullptr) {
-        V::load(y_shared + t * d + c, acc);
+    float acc[kCombineVecs][n];
+#pragma unroll
+    for (int v = 0; v < kCombineVecs; ++v) {
+      const int c = c0 + (v * 32 + lane) * n;
+      if (y_shared != nullptr && c < d) {
+        V::load(y_shared + t * d + c, acc[v]);
       } else {
 #pragma unroll
-        for (int i = 0; i < n; ++i) acc[i] = 0.f;
+        for (int i = 0; i < n; ++i) acc[v][i] = 0.f;
       }
-      for (int k = 0; k < K; ++k) {
-        float y[n];
-        V::load(y_perm + rows[k] * d + c, y);
+    }
+    for (int k = 0; k < K; ++k) {
+      const int64_t row = __shfl_sync(0xffffffffu, my_row, k);
+      const float g = __shfl_sync(0xffffffffu, my_g, k);
 #pragma unroll
-        for (int i = 0; i < n; ++i) acc[i] = fmaf(g[k], y[i], acc[i]);
+      for (int v = 0; v < kCombineVecs; ++v) {
+        const int c = c0 + (v * 32 + lane) * n;
+        if (c < d) {
+          float y[n];
+          V::load(y_perm + row * d + c, y);
+#pragma unroll
+          for (int i = 0; i < n; ++i) acc[v][i] = fmaf(g, y[i], acc[v][i]);
+        }
       }
-      V::store(out + t * d + c, acc);
+    }
+#pragma unroll
+    for (int v = 0; v < kCombineVecs; ++v) {
+      const int c = c0 + (v * 32 + lane) * n;
+      if (c < d) V::store(out + t * d + c, acc[v]);
     }
   }
 }
@@ -251,12 +271,15 @@ cudaError_t launch_combine(const moe_cfg_t& c, const void* y_perm, const void* y
                            const int32_t* row_of_slot, const float* topk_w, void* out,
                            cudaStream_t st) {
   const int64_t n_rows = static_cast<int64_t>(c.T) * c.K;
+  const int per = (c.dtype == MOE_DTYPE_FP32 ? 4 : 8) * 32 * kCombineVecs;
+  const int64_t items = static_cast<int64_t>(c.T) * ((c.d + per - 1) / per);
+  const int grid = row_grid(items);
   if (c.dtype == MOE_DTYPE_FP32)
-    combine_kernel<float><<<row_grid(c.T), kRowWarps * 32, 0, st>>>(
+    combine_kernel<float><<<grid, kRowWarps * 32, 0, st>>>(
         static_cast<const float*>(y_perm), static_cast<const float*>(y_shared), row_of_slot,
         topk_w, static_cast<float*>(out), c.T, c.K, c.d, n_rows);
   else
-    combine_kernel<__nv_bfloat16><<<row_grid(c.T), kRowWarps * 32, 0, st>>>(
+    combine_kernel<__nv_bfloat16><<<grid, kRowWarps * 32, 0, st>>>(
         static_cast<const __nv_bfloat16*>(y_perm), static_cast<const __nv_bfloat16*>(y_shared),
         row_of_slot, topk_w, static_cast<__nv_bfloat16*>(out), c.T, c.K, c.d, n_rows);
   return cudaGetLastError();

@@ -22,6 +22,7 @@ size_t route_scratch_bytes(const moe_cfg_t& c, bool need_affinity) {
   const size_t ntile = ceil_div(c.T, kRouteTile);
   size_t b = align_up(ntile * c.E * sizeof(int32_t), 256);
   if (need_affinity) b += align_up(static_cast<size_t>(c.T) * c.E * sizeof(float), 256);
+  if (c.dtype != MOE_DTYPE_FP32) b += router_tc_scratch_bytes(c);
   return b;
 }
 
@@ -31,7 +32,11 @@ RouteScratch route_scratch_carve(const moe_cfg_t& c, void* ws, bool need_affinit
   const size_t ntile = ceil_div(c.T, kRouteTile);
   r.tile_counts = reinterpret_cast<int32_t*>(p);
   p += align_up(ntile * c.E * sizeof(int32_t), 256);
-  if (need_affinity) r.affinity = reinterpret_cast<float*>(p);
+  if (need_affinity) {
+    r.affinity = reinterpret_cast<float*>(p);
+    p += align_up(static_cast<size_t>(c.T) * c.E * sizeof(float), 256);
+  }
+  if (c.dtype != MOE_DTYPE_FP32) r.router = p;
   return r;
 }
 
@@ -94,15 +99,14 @@ __global__ void __launch_bounds__(256) router_affinity_kernel(const TX* __restri
   }
 }
 
+// fp32 token rows: CUDA-core product.  bf16 token rows: tensor cores with
+// the centroids split into three bf16 terms (router_sm100.cu).
 cudaError_t launch_router_affinity(const moe_cfg_t& c, const void* x, const float* w,
-                                   float* affinity, cudaStream_t st) {
+                                   float* affinity, const RouteScratch& rs, cudaStream_t st) {
+  if (c.dtype != MOE_DTYPE_FP32) return launch_router_tc(c, x, w, affinity, rs.router, st);
   dim3 grid(ceil_div(c.E, kAffBN), ceil_div(c.T, kAffBM));
-  if (c.dtype == MOE_DTYPE_FP32)
-    router_affinity_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), w,
-                                                        affinity, c.T, c.E, c.d);
-  else
-    router_affinity_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), w, affinity, c.T, c.E, c.d);
+  router_affinity_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), w, affinity,
+                                                      c.T, c.E, c.d);
   return cudaGetLastError();
 }
 
@@ -121,13 +125,20 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
   }
 }
 
-constexpr int kSelWarps = 8;
 constexpr int kMaxTopn = 8;
 
-// One block per 32-token tile, one warp per 4 tokens.  Per token: the
-// biased scores go to shared memory; lane g scores group g; the kept groups
-// and then the K experts come from repeated warp arg-max reductions.
-__global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
+// Warps per selection block: one token per warp when the per-warp buffers
+// (2 E floats) fit in 64 KiB, fewer warps (several tokens each) otherwise.
+static int select_warps(int E) {
+  int w = 32;
+  while (w > 1 && static_cast<size_t>(w) * 2 * E * sizeof(float) > 64 * 1024) w >>= 1;
+  return w;
+}
+
+// One block per 32-token tile.  Per token: the biased scores go to shared
+// memory; lane g scores group g; the kept groups and then the K experts come
+// from repeated warp arg-max reductions.
+__global__ void __launch_bounds__(1024) route_select_kernel(
     const float* __restrict__ affinity, const float* __restrict__ bias,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
     int32_t* __restrict__ local_rank, int32_t* __restrict__ tile_counts, int T, int E,
@@ -135,7 +146,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
   extern __shared__ float sel_smem[];
   float* biased = sel_smem + (threadIdx.x / 32) * 2 * E;  // per warp [E]
   float* sval = biased + E;                               // per warp [E]
-  uint32_t* mask = reinterpret_cast<uint32_t*>(sel_smem + kSelWarps * 2 * E);  // [E]
+  const int n_warps = blockDim.x / 32;
+  uint32_t* mask = reinterpret_cast<uint32_t*>(sel_smem + n_warps * 2 * E);  // [E]
   int32_t* chosen = reinterpret_cast<int32_t*>(mask + E);                     // [32][K]
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   const int tile = blockIdx.x;
@@ -145,7 +157,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
   for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0u;
   __syncthreads();
 
-  for (int tl = warp; tl < kRouteTile; tl += kSelWarps) {
+  for (int tl = warp; tl < kRouteTile; tl += n_warps) {
     const int t = tile * kRouteTile + tl;
     if (t >= T) break;
     const float* srow = affinity + static_cast<size_t>(t) * E;
@@ -233,7 +245,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
 cudaError_t launch_route_select(const moe_cfg_t& c, const float* affinity, const float* bias,
                                 int32_t* topk_idx, float* topk_w, int32_t* local_rank,
                                 int32_t* tile_counts, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(kSelWarps) * 2 * c.E * sizeof(float) +
+  const int warps = select_warps(c.E);
+  const size_t smem = static_cast<size_t>(warps) * 2 * c.E * sizeof(float) +
                       static_cast<size_t>(c.E) * sizeof(uint32_t) +
                       static_cast<size_t>(kRouteTile) * c.K * sizeof(int32_t);
   if (smem > 48 * 1024) {
@@ -242,7 +255,7 @@ cudaError_t launch_route_select(const moe_cfg_t& c, const float* affinity, const
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  route_select_kernel<<<ceil_div(c.T, kRouteTile), kSelWarps * 32, smem, st>>>(
+  route_select_kernel<<<ceil_div(c.T, kRouteTile), warps * 32, smem, st>>>(
       affinity, bias, topk_idx, topk_w, local_rank, tile_counts, c.T, c.E, c.n_groups,
       c.topk_groups, c.K, c.group_score_topn, c.route_scale);
   return cudaGetLastError();

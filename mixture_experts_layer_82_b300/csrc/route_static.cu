@@ -14,7 +14,7 @@
 
 namespace moe {
 
-constexpr size_t kStaticScratchBytes = size_t{16} << 20;  // 16 MiB
+constexpr size_t kStaticScratchBytes = size_t{32} << 20;  // 32 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_route_scratch[kStaticScratchBytes];
@@ -70,7 +70,7 @@ extern "C" moe_status_t moe_route_static_scratch(
   const float* aff = affinity_in;
   if (aff == nullptr) {
     float* dst = affinity_out != nullptr ? affinity_out : rs.affinity;
-    if (launch_router_affinity(c, x, router_w, dst, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_router_affinity(c, x, router_w, dst, rs, s) != cudaSuccess) return MOE_ERR_CUDA;
     aff = dst;
   } else if (affinity_out != nullptr && affinity_out != affinity_in) {
     if (cudaMemcpyAsync(affinity_out, affinity_in, static_cast<size_t>(c.T) * c.E * sizeof(float),
