@@ -1,10 +1,516 @@
-// FP8 E4M3 grouped expert GEMMs (fine-grained scales).  Not built yet: the
-// FP8 kind is rejected by the host checks until this kernel exists.
+// Grouped expert GEMMs in FP8 E4M3 with fine-grained scales, on the
+// 5th-generation tensor cores (tcgen05 + TMEM) fed by TMA.
+//
+// "DeepSeek-V3 Technical Report":
+//   - fine-grained quantisation paragraph / Appendix B.2: activations carry
+//     one fp32 scale per 1 x 128 tile, weights one per 128 x 128 block;
+//   - increased-precision accumulation paragraph: every N_C = 128 elements
+//     of the reduction, the tensor-core partial sum is moved to fp32 CUDA
+//     -core registers, where the scales are applied.
+// Here the reduction is cut in 128-element K blocks (one pipeline stage).
+// The tensor cores write each block's partial product into one of two TMEM
+// partials (alternating, so the MMAs of block kb+1 run while block kb is
+// promoted); eight epilogue warps read the partial (tcgen05.ld), multiply
+// it by sa[row, kb] * sw[col block, kb] and add it to fp32 registers.
+//
+// Two launches per layer, one persistent kernel each:
+//   gate/up: per 128 x 256 tile the 256 MMA columns are 128 rows of W1 and
+//            the matching 128 rows of W3; the epilogue forms
+//            h = silu(a) * b for 128 h columns and quantises h again in
+//            1 x 128 tiles (codes + fp32 scales) for the down projection;
+//   down:    y = h W2^T per 128 x 256 tile, bf16 output.
+// The work list and its order are those of the bf16 kernel: every
+// (group, M tile, N tile) of the routed experts, then the shared class;
+// M varies fastest inside a group so concurrently running CTAs share each
+// weight tile through L2.
+//
+// Roles (320 threads, one CTA per SM):
+//   warp 0      TMA producer: A and B tiles into a 4-stage ring (48 KB/stage)
+//   warp 1      allocates 512 TMEM columns; one thread issues
+//               tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32), 4 per block
+//   warps 2..9  promotion + epilogue.  Warp w reads TMEM lanes
+//               32*(w%4)..+31 (its rows); warps 2..5 own column half 0,
+//               warps 6..9 half 1.  Gate/up: a half is 64 gate columns and
+//               the 64 matching up columns, so SwiGLU needs no exchange;
+//               the two halves of a row swap one amax through shared memory
+//               for the 1 x 128 requantisation.  Down: a half is one
+//               128-column weight block.
+// Every wait is bounded; a wait that gives up sets the error word and the
+// block-wide abort flag, so all roles leave, drain their own copies in
+// flight and free TMEM.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
-cudaError_t launch_experts_fp8(const ExpertsArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace fp8gemm {
+
+constexpr int BM = 128, BN = 256, BK = 128;  // BK bytes = one 128-byte swizzle row = one scale block
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;             // 16 KiB
+constexpr int B_BYTES = BN * BK;             // 32 KiB
+constexpr int B_HALF_BYTES = B_BYTES / 2;    // one 128-row box
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr int MAX_GROUPS = 1025;             // 1024 routed experts + the shared class
+constexpr uint32_t TMEM_COLS = 512;          // two 256-column partials
+constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, BN);  // E4M3 x E4M3 -> fp32
+
+enum { GATEUP = 0, DOWN = 1 };
+
+struct ClassDesc {
+  void* out;              // gate/up: E4M3 h codes [rows, n_out]; down: bf16 y [rows, n_out]
+  float* out_scales;      // gate/up: h scales [rows, n_out / 128]; down: unused
+  const float* a_scales;  // [rows, k_dim / 128]
+  const float* w_scales;  // block scales of the class's weight matrices
+  int n_out;              // output columns (row stride of out)
+  int k_dim;              // reduction length
+};
+
+struct Params {
+  CUtensorMap a_map[2];  // [0] routed rows, [1] shared rows
+  CUtensorMap b_map[2];  // [0] routed weights, [1] shared weights
+  ClassDesc cls[2];
+  const int32_t* offsets;
+  int E;
+  int T;
+  int has_shared;
+  int inter;  // I
+  int d;
+};
+
+struct Smem {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t pfull[2];
+  uint64_t pempty[2];
+  uint64_t xch;
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+  int n_groups;
+  float red[2][2][BM];         // [tile parity][column half][row]: |h| maxima
+  int gstart[MAX_GROUPS + 1];  // first tile of every group
+  int mtiles[MAX_GROUPS];      // M tiles of every group
+};
+
+constexpr size_t kRingBytes = static_cast<size_t>(STAGES) * (A_BYTES + B_BYTES);
+constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(Smem);
+
+struct Tile {
+  int cls;     // 0 routed, 1 shared
+  int group;   // routed expert index (cls 0)
+  int row0;    // first row of the group in its class's row space
+  int rows;    // valid rows of the group
+  int mt, nt;  // tile coordinates inside the group
+};
+
+template <int MODE>
+__device__ __forceinline__ int out_tile_cols() { return MODE == GATEUP ? BN / 2 : BN; }
+
+template <int MODE>
+__device__ __forceinline__ int n_tiles_of(const Params& p, int cls) {
+  return ceil_div(p.cls[cls].n_out, out_tile_cols<MODE>());
+}
+
+template <int MODE>
+__device__ void build_tile_table(const Params& p, Smem& s) {
+  const int lane = threadIdx.x % 32;
+  const int G = p.E + (p.has_shared ? 1 : 0);
+  const int per = ceil_div(G, 32);
+  const int g0 = lane * per, g1 = min(G, g0 + per);
+  int sum = 0;
+  for (int g = g0; g < g1; ++g) {
+    int rows, cls;
+    if (g < p.E) { rows = p.offsets[g + 1] - p.offsets[g]; cls = 0; }
+    else { rows = p.T; cls = 1; }
+    const int mt = ceil_div(max(rows, 0), BM);
+    s.mtiles[g] = mt;
+    sum += mt * n_tiles_of<MODE>(p, cls);
+  }
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int run = incl - sum;
+  for (int g = g0; g < g1; ++g) {
+    s.gstart[g] = run;
+    const int cls = g < p.E ? 0 : 1;
+    run += s.mtiles[g] * n_tiles_of<MODE>(p, cls);
+  }
+  if (lane == 31) { s.gstart[G] = incl; s.n_groups = G; }
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int t) {
+  int lo = 0, hi = s.n_groups;  // gstart[lo] <= t < gstart[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s.gstart[mid] <= t) lo = mid; else hi = mid;
+  }
+  Tile tl;
+  tl.cls = lo < p.E ? 0 : 1;
+  tl.group = lo;
+  const int local = t - s.gstart[lo];
+  const int mt_count = s.mtiles[lo];
+  tl.mt = local % mt_count;
+  tl.nt = local / mt_count;
+  if (tl.cls == 0) { tl.row0 = p.offsets[lo]; tl.rows = p.offsets[lo + 1] - tl.row0; }
+  else { tl.row0 = 0; tl.rows = p.T; }
+  return tl;
+}
+
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+  int never = 0;
+  return mbar_wait(bar, parity, &never);
+}
+
+// Weight-block scales of one K block for the epilogue thread's columns.
+// Gate/up: [0] the W1 block, [1] the matching W3 block.  Down: [0] the
+// thread's 128-column block of W2 ([1] unused); 0 for a block past d.
+template <int MODE>
+__device__ __forceinline__ void weight_scales(const Params& p, const Tile& tl, int hf, int kb,
+                                              float& s0, float& s1) {
+  const ClassDesc& cd = p.cls[tl.cls];
+  const int I = p.inter;
+  if (MODE == GATEUP) {
+    const int n0 = tl.nt * (BN / 2);
+    const int mat = tl.cls == 0 ? tl.group : n0 / I;
+    const int i0 = n0 % I;
+    const int kbs = p.d / BK;
+    const int nbs = 2 * I / BK;
+    const float* w = cd.w_scales + static_cast<size_t>(mat) * nbs * kbs;
+    s0 = __ldg(w + static_cast<size_t>(i0 / BK) * kbs + kb);
+    s1 = __ldg(w + static_cast<size_t>((I + i0) / BK) * kbs + kb);
+  } else {
+    const int k0 = kb * BK;
+    const int mat = tl.cls == 0 ? tl.group : k0 / I;
+    const int kl = (k0 % I) / BK;
+    const int nb = tl.nt * 2 + hf;
+    const int nbs = p.d / BK;
+    const int kbs = I / BK;
+    s0 = nb < nbs ? __ldg(cd.w_scales + (static_cast<size_t>(mat) * nbs + nb) * kbs + kl) : 0.f;
+    s1 = 0.f;
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Smem& s = *reinterpret_cast<Smem*>(ring + kRingBytes);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  volatile int* abort_flag = &s.abort;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) { tma_prefetch_desc(&p.a_map[i]); tma_prefetch_desc(&p.b_map[i]); }
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&s.pfull[i], 1); mbar_init(&s.pempty[i], EPI_WARPS); }
+    mbar_init(&s.xch, EPI_WARPS * 32);
+    mbar_init(&s.done, 1);
+    s.abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (warp == 2) build_tile_table<MODE>(p, s);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s.tmem_base;
+  const int total = s.gstart[s.n_groups];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_a = l2_policy_evict_last();
+      const uint64_t pol_b = l2_policy_evict_normal();
+      uint32_t stage = 0, phase = 0;
+      int issued = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const Tile tl = decode_tile<MODE>(p, s, t);
+        const ClassDesc& cd = p.cls[tl.cls];
+        const int nk = cd.k_dim / BK;
+        const int a_row = tl.row0 + tl.mt * BM;
+        const CUtensorMap* am = &p.a_map[tl.cls];
+        const CUtensorMap* bm = &p.b_map[tl.cls];
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) break;
+          uint8_t* sa = ring + stage * A_BYTES;
+          uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
+          mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
+          tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
+          int bx, by0, by1;
+          if (MODE == GATEUP) {
+            const int n0 = tl.nt * (BN / 2);
+            const int sh = n0 / p.inter, i0 = n0 % p.inter;
+            const int base = (tl.cls == 0 ? tl.group : sh) * 2 * p.inter;
+            bx = kb * BK;
+            by0 = base + i0;
+            by1 = base + p.inter + i0;
+          } else {
+            const int k0 = kb * BK;
+            const int sh = k0 / p.inter;
+            const int ex = tl.cls == 0 ? tl.group : sh;
+            bx = tl.cls == 0 ? k0 : k0 % p.inter;
+            by0 = ex * p.d + tl.nt * BN;
+            by1 = by0 + BN / 2;
+          }
+          tma_load_2d(sb, bm, &s.full[stage], bx, by0, pol_b);
+          tma_load_2d(sb + B_HALF_BYTES, bm, &s.full[stage], bx, by1, pol_b);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int i = 0; i < STAGES && i < issued; ++i) {
+        if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
+        drain_wait(&s.full[stage], phase);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, pc = 0;
+      bool any = false, ok = true;
+      for (int t = blockIdx.x; t < total && ok && !*abort_flag; t += gridDim.x) {
+        const Tile tl = decode_tile<MODE>(p, s, t);
+        const int nk = p.cls[tl.cls].k_dim / BK;
+        for (int kb = 0; kb < nk; ++kb, ++pc) {
+          const int buf = pc & 1;
+          if (!mbar_wait(&s.pempty[buf], ((pc >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (!mbar_wait(&s.full[stage], phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+          const uint32_t a0 = smem_u32(ring + stage * A_BYTES);
+          const uint32_t b0 = smem_u32(ring + STAGES * A_BYTES + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_fp8_ss(d_tmem, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32),
+                       IDESC, k != 0 ? 1u : 0u);
+          any = true;
+          mma_commit(&s.empty[stage]);
+          mma_commit(&s.pfull[buf]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (any) {
+        mma_commit(&s.done);
+        drain_wait(&s.done, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------- promotion + epilogue
+    const int q = warp & 3;              // TMEM lane quarter of this warp
+    const int hf = (warp - 2) >> 2;      // column half
+    const int r_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t pc = 0;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const Tile tl = decode_tile<MODE>(p, s, t);
+      const ClassDesc& cd = p.cls[tl.cls];
+      const int nk = cd.k_dim / BK;
+      const int m = tl.mt * BM + r_in_tile;
+      const bool valid = m < tl.rows;
+      const size_t grow = static_cast<size_t>(tl.row0) + (valid ? m : 0);
+      const float* sa_row = cd.a_scales + grow * nk;
+      float acc[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+      bool ok = true;
+      float sa_next = valid ? __ldg(sa_row) : 0.f;
+      float s0n, s1n;
+      weight_scales<MODE>(p, tl, hf, 0, s0n, s1n);
+      for (int kb = 0; kb < nk; ++kb, ++pc) {
+        const float sa = sa_next;
+        const float s0 = s0n, s1 = s1n;
+        if (kb + 1 < nk) {
+          sa_next = valid ? __ldg(sa_row + kb + 1) : 0.f;
+          weight_scales<MODE>(p, tl, hf, kb + 1, s0n, s1n);
+        }
+        const int buf = pc & 1;
+        if (!mbar_wait(&s.pfull[buf], (pc >> 1) & 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t taddr = lane_addr + static_cast<uint32_t>(buf * BN);
+        if (MODE == GATEUP) {
+          const float sg = sa * s0, su = sa * s1;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float g[8], u[8];
+            tmem_ld8(taddr + hf * 64 + j * 8, g);
+            tmem_ld8(taddr + BN / 2 + hf * 64 + j * 8, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              acc[j * 8 + i] = fmaf(g[i], sg, acc[j * 8 + i]);
+              acc[64 + j * 8 + i] = fmaf(u[i], su, acc[64 + j * 8 + i]);
+            }
+          }
+        } else {
+          const float sc = sa * s0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float v[16];
+            tmem_ld16(taddr + hf * 128 + j * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(v[i], sc, acc[j * 16 + i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.pempty[buf]);
+      }
+      if (!ok) break;
+
+      if (MODE == GATEUP) {
+        // h = silu(a) * b, then one E4M3 scale per row and 128 h columns
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float h = silu_f(acc[i]) * acc[64 + i];
+          acc[i] = h;
+          amax = fmaxf(amax, fabsf(h));
+        }
+        const int xb = it & 1;
+        s.red[xb][hf][r_in_tile] = amax;
+        mbar_arrive(&s.xch);
+        if (!mbar_wait(&s.xch, static_cast<uint32_t>(it) & 1u, abort_flag)) break;
+        amax = fmaxf(amax, s.red[xb][hf ^ 1][r_in_tile]);
+        const float scale = fp8_scale_of(amax);
+        if (valid) {
+          const int n0 = tl.nt * (BN / 2);
+          uint8_t* orow = static_cast<uint8_t*>(cd.out) + grow * cd.n_out + n0 + hf * 64;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = quant4_e4m3(acc[v * 16 + 0], acc[v * 16 + 1], acc[v * 16 + 2], acc[v * 16 + 3], scale);
+            w.y = quant4_e4m3(acc[v * 16 + 4], acc[v * 16 + 5], acc[v * 16 + 6], acc[v * 16 + 7], scale);
+            w.z = quant4_e4m3(acc[v * 16 + 8], acc[v * 16 + 9], acc[v * 16 + 10], acc[v * 16 + 11], scale);
+            w.w = quant4_e4m3(acc[v * 16 + 12], acc[v * 16 + 13], acc[v * 16 + 14], acc[v * 16 + 15], scale);
+            reinterpret_cast<uint4*>(orow)[v] = w;
+          }
+          if (hf == 0) cd.out_scales[grow * (cd.n_out / BK) + n0 / BK] = scale;
+        }
+      } else {
+        const int n_base = tl.nt * BN + hf * 128;
+        if (valid) {
+          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(cd.out) + grow * cd.n_out + n_base;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (n_base + c * 16 < cd.n_out) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+              dst[0] = make_uint4(pack_bf16x2(acc[c * 16 + 0], acc[c * 16 + 1]),
+                                  pack_bf16x2(acc[c * 16 + 2], acc[c * 16 + 3]),
+                                  pack_bf16x2(acc[c * 16 + 4], acc[c * 16 + 5]),
+                                  pack_bf16x2(acc[c * 16 + 6], acc[c * 16 + 7]));
+              dst[1] = make_uint4(pack_bf16x2(acc[c * 16 + 8], acc[c * 16 + 9]),
+                                  pack_bf16x2(acc[c * 16 + 10], acc[c * 16 + 11]),
+                                  pack_bf16x2(acc[c * 16 + 12], acc[c * 16 + 13]),
+                                  pack_bf16x2(acc[c * 16 + 14], acc[c * 16 + 15]));
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace fp8gemm
+
+template <int MODE>
+static cudaError_t launch_fp8_gemm(const fp8gemm::Params& prm, cudaStream_t st) {
+  using namespace fp8gemm;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(experts_fp8_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  experts_fp8_kernel<MODE><<<sm_count(), THREADS, kSmemBytes, st>>>(prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t st) {
+  using namespace fp8gemm;
+  const moe_cfg_t& c = *a.cfg;
+  const int64_t tk = static_cast<int64_t>(c.T) * c.K;
+  const int I = c.inter, Ns = c.n_shared;
+  uint8_t* h_routed = static_cast<uint8_t*>(a.h);
+  uint8_t* h_shared = h_routed + tk * I;
+  float* hs_routed = a.h_scales;
+  float* hs_shared = a.h_scales + tk * (I / BK);
+  const bool has_shared = Ns > 0;
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
+
+  // ---- gate/up: A = x_perm / x_q (E4M3), B = W13 (E4M3)
+  Params g{};
+  g.offsets = a.offsets; g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
+  g.inter = I; g.d = c.d;
+  CUresult r = encode_tensor_map_2d(&g.a_map[0], U8, const_cast<void*>(a.x_perm), c.d, tk,
+                                    static_cast<uint64_t>(c.d), BK, BM, SW);
+  if (r == CUDA_SUCCESS)
+    r = encode_tensor_map_2d(&g.b_map[0], U8, const_cast<void*>(a.w13), c.d,
+                             static_cast<uint64_t>(c.E) * 2 * I, static_cast<uint64_t>(c.d), BK,
+                             BN / 2, SW);
+  if (r == CUDA_SUCCESS && has_shared) {
+    r = encode_tensor_map_2d(&g.a_map[1], U8, const_cast<void*>(a.x), c.d, c.T,
+                             static_cast<uint64_t>(c.d), BK, BM, SW);
+    if (r == CUDA_SUCCESS)
+      r = encode_tensor_map_2d(&g.b_map[1], U8, const_cast<void*>(a.ws13), c.d,
+                               static_cast<uint64_t>(Ns) * 2 * I, static_cast<uint64_t>(c.d), BK,
+                               BN / 2, SW);
+  } else {
+    g.a_map[1] = g.a_map[0];
+    g.b_map[1] = g.b_map[0];
+  }
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  g.cls[0] = ClassDesc{h_routed, hs_routed, a.x_perm_scales, a.w13_scales, I, c.d};
+  g.cls[1] = ClassDesc{h_shared, hs_shared, has_shared ? a.x_scales : a.x_perm_scales,
+                       has_shared ? a.ws13_scales : a.w13_scales, Ns * I, c.d};
+  cudaError_t e = launch_fp8_gemm<GATEUP>(g, st);
+  if (e != cudaSuccess) return e;
+
+  // ---- down: A = h codes, B = W2 (E4M3)
+  Params dn = g;
+  r = encode_tensor_map_2d(&dn.a_map[0], U8, h_routed, I, tk, static_cast<uint64_t>(I), BK, BM, SW);
+  if (r == CUDA_SUCCESS)
+    r = encode_tensor_map_2d(&dn.b_map[0], U8, const_cast<void*>(a.w2), I,
+                             static_cast<uint64_t>(c.E) * c.d, static_cast<uint64_t>(I), BK,
+                             BN / 2, SW);
+  if (r == CUDA_SUCCESS && has_shared) {
+    r = encode_tensor_map_2d(&dn.a_map[1], U8, h_shared, static_cast<uint64_t>(Ns) * I, c.T,
+                             static_cast<uint64_t>(Ns) * I, BK, BM, SW);
+    if (r == CUDA_SUCCESS)
+      r = encode_tensor_map_2d(&dn.b_map[1], U8, const_cast<void*>(a.ws2), I,
+                               static_cast<uint64_t>(Ns) * c.d, static_cast<uint64_t>(I), BK,
+                               BN / 2, SW);
+  } else {
+    dn.a_map[1] = dn.a_map[0];
+    dn.b_map[1] = dn.b_map[0];
+  }
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  dn.cls[0] = ClassDesc{a.y_perm, nullptr, hs_routed, a.w2_scales, c.d, I};
+  dn.cls[1] = ClassDesc{has_shared ? a.y_shared : a.y_perm, nullptr,
+                        has_shared ? hs_shared : hs_routed,
+                        has_shared ? a.ws2_scales : a.w2_scales, c.d, Ns > 0 ? Ns * I : I};
+  return launch_fp8_gemm<DOWN>(dn, st);
+}
 
 }  // namespace moe

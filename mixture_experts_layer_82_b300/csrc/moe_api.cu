@@ -60,7 +60,6 @@ moe_status_t moe_check_cfg(const moe_cfg_t* c) {
     if (m_tiles >= 65535) return MOE_ERR_SHAPE;
   } else {
     if (c->d % 128 != 0 || c->inter % 128 != 0) return MOE_ERR_SHAPE;
-    if (c->dtype == MOE_DTYPE_FP8_E4M3) return MOE_ERR_SHAPE;  // kernel not built yet
   }
   return MOE_OK;
 }

@@ -39,3 +39,8 @@ from .fp8 import (  # noqa: F401
     dequantize_weight_128x128,
     fp8_linear,
 )
+from .moe_fp8 import (  # noqa: F401
+    fp8_swiglu_ffn,
+    moe_layer_forward_fp8,
+    moe_layer_tokens_fp8,
+)
