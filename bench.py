@@ -425,9 +425,25 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
+                    help="override a field of the workload's shape (a reduced case for "
+                         "profiling, e.g. --set E=32 --set router=gaussian)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # timing rule: at least 3 untimed steps
     shape = CONFIGS[args.workload]
+    if args.set:
+        from dataclasses import fields
+        from moe_synth import shape_with
+        types = {f.name: f.type for f in fields(shape)}
+        kw = {}
+        for item in args.set:
+            k, v = item.split("=", 1)
+            if k not in types:
+                ap.error(f"--set: unknown shape field {k!r}")
+            t = types[k] if not isinstance(types[k], str) else {"int": int, "float": float,
+                                                                 "str": str}[types[k]]
+            kw[k] = t(v)
+        shape = shape_with(shape, **kw)
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":

@@ -24,17 +24,23 @@
 // M varies fastest inside a group so concurrently running CTAs share each
 // weight tile through L2.
 //
-// Roles (320 threads, one CTA per SM):
+// Roles (384 threads = 3 warpgroups, one CTA per SM):
 //   warp 0      TMA producer: A and B tiles into a 4-stage ring (48 KB/stage)
-//   warp 1      allocates 512 TMEM columns; one thread issues
-//               tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32), 4 per block
-//   warps 2..9  promotion + epilogue.  Warp w reads TMEM lanes
-//               32*(w%4)..+31 (its rows); warps 2..5 own column half 0,
-//               warps 6..9 half 1.  Gate/up: a half is 64 gate columns and
+//   warp 1      allocates 512 TMEM columns; warps 1 and 2 issue
+//               tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32), 4 per block,
+//               one thread each, for alternate K blocks
+//   warp 3      idle
+//   warps 4..11 promotion + epilogue.  Warp w reads TMEM lanes
+//               32*(w%4)..+31 (its rows); warpgroup 1 owns column half 0,
+//               warpgroup 2 half 1.  Gate/up: a half is 64 gate columns and
 //               the 64 matching up columns, so SwiGLU needs no exchange;
 //               the two halves of a row swap one amax through shared memory
 //               for the 1 x 128 requantisation.  Down: a half is one
 //               128-column weight block.
+// Registers: launched at 168 per thread; warpgroup 0 gives its share down
+// to 56 and the two epilogue warpgroups take 224 each (4*32*56 +
+// 8*32*224 = 384*168), room for 128 fp32 accumulators, a 32-column batch
+// of TMEM loads and the scales, which are loaded two K blocks ahead.
 // Every wait is bounded; a wait that gives up sets the error word and the
 // block-wide abort flag, so all roles leave, drain their own copies in
 // flight and free TMEM.
@@ -53,7 +59,11 @@ constexpr int A_BYTES = BM * BK;             // 16 KiB
 constexpr int B_BYTES = BN * BK;             // 32 KiB
 constexpr int B_HALF_BYTES = B_BYTES / 2;    // one 128-row box
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr int EPI_WARP0 = 4;                 // first epilogue warp (warpgroup 1)
+constexpr int THREADS = 128 + EPI_WARPS * 32;
+constexpr uint32_t REGS_LOW = 56, REGS_HIGH = 224;  // after setmaxnreg
+static_assert(4 * 32 * REGS_LOW + EPI_WARPS * 32 * REGS_HIGH <= THREADS * 168,
+              "register split above the launch allocation");
 constexpr int MAX_GROUPS = 1025;             // 1024 routed experts + the shared class
 constexpr uint32_t TMEM_COLS = 512;          // two 256-column partials
 constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, BN);  // E4M3 x E4M3 -> fp32
@@ -87,7 +97,7 @@ struct Smem {
   uint64_t pfull[2];
   uint64_t pempty[2];
   uint64_t xch;
-  uint64_t done;
+  uint64_t done[2];
   uint32_t tmem_base;
   int abort;
   int n_groups;
@@ -169,33 +179,112 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return mbar_wait(bar, parity, &never);
 }
 
-// Weight-block scales of one K block for the epilogue thread's columns.
-// Gate/up: [0] the W1 block, [1] the matching W3 block.  Down: [0] the
-// thread's 128-column block of W2 ([1] unused); 0 for a block past d.
+// Scales of the epilogue thread's row and columns, K block after K block.
+// Activation: sa[row, kb] (0 for a row past the segment).  Gate/up: the
+// W1 block and the matching W3 block of the tile's 128 h columns.  Down:
+// the thread's 128-column block of W2 (0 for a block past d); the shared
+// class walks K over its N_s matrices, so the cursor steps to the next
+// matrix every I/128 blocks.  Loads are issued two K blocks before use.
 template <int MODE>
-__device__ __forceinline__ void weight_scales(const Params& p, const Tile& tl, int hf, int kb,
-                                              float& s0, float& s1) {
-  const ClassDesc& cd = p.cls[tl.cls];
-  const int I = p.inter;
-  if (MODE == GATEUP) {
-    const int n0 = tl.nt * (BN / 2);
-    const int mat = tl.cls == 0 ? tl.group : n0 / I;
-    const int i0 = n0 % I;
-    const int kbs = p.d / BK;
-    const int nbs = 2 * I / BK;
-    const float* w = cd.w_scales + static_cast<size_t>(mat) * nbs * kbs;
-    s0 = __ldg(w + static_cast<size_t>(i0 / BK) * kbs + kb);
-    s1 = __ldg(w + static_cast<size_t>((I + i0) / BK) * kbs + kb);
-  } else {
-    const int k0 = kb * BK;
-    const int mat = tl.cls == 0 ? tl.group : k0 / I;
-    const int kl = (k0 % I) / BK;
-    const int nb = tl.nt * 2 + hf;
-    const int nbs = p.d / BK;
-    const int kbs = I / BK;
-    s0 = nb < nbs ? __ldg(cd.w_scales + (static_cast<size_t>(mat) * nbs + nb) * kbs + kl) : 0.f;
-    s1 = 0.f;
+struct ScaleCursor {
+  const float* a;   // activation scales of the row, next block to load
+  const float* w0;  // gate/up: W1 block row; down: W2 block at kl = 0 of the current matrix
+  const float* w1;  // gate/up: W3 block row
+  int kl;           // next K block (gate/up: absolute; down: inside the current matrix)
+  int kbs;          // down: K blocks per matrix
+  int mat_floats;   // down: scale floats per matrix
+  bool row_ok, col_ok;
+
+  __device__ __forceinline__ void init(const Params& p, const Tile& tl, int hf, bool valid,
+                                       size_t grow) {
+    const ClassDesc& cd = p.cls[tl.cls];
+    const int I = p.inter;
+    a = cd.a_scales + grow * (cd.k_dim / BK);
+    row_ok = valid;
+    kl = 0;
+    if (MODE == GATEUP) {
+      const int n0 = tl.nt * (BN / 2);
+      const int mat = tl.cls == 0 ? tl.group : n0 / I;
+      const int i0 = n0 % I;
+      const int kd = p.d / BK, nbs = 2 * I / BK;
+      const float* base = cd.w_scales + static_cast<size_t>(mat) * nbs * kd;
+      w0 = base + static_cast<size_t>(i0 / BK) * kd;
+      w1 = base + static_cast<size_t>((I + i0) / BK) * kd;
+      col_ok = true;
+    } else {
+      const int nbs = p.d / BK;
+      const int nb = tl.nt * 2 + hf;
+      kbs = I / BK;
+      mat_floats = nbs * kbs;
+      col_ok = nb < nbs;
+      const int mat = tl.cls == 0 ? tl.group : 0;
+      w0 = cd.w_scales + (static_cast<size_t>(mat) * nbs + (col_ok ? nb : 0)) * kbs;
+      w1 = w0;
+    }
   }
+
+  // Loads the next K block's scales and advances.
+  __device__ __forceinline__ void next(float& sa, float& s0, float& s1) {
+    sa = row_ok ? __ldg(a) : 0.f;
+    ++a;
+    if (MODE == GATEUP) {
+      s0 = __ldg(w0 + kl);
+      s1 = __ldg(w1 + kl);
+      ++kl;
+    } else {
+      s0 = col_ok ? __ldg(w0 + kl) : 0.f;
+      s1 = 0.f;
+      if (++kl == kbs) { kl = 0; w0 += mat_floats; }
+    }
+  }
+};
+
+// Promotion of one K block: waits for its TMEM partial, adds
+// partial * sa * sw to the fp32 accumulators and hands the partial back to
+// the MMA thread.  Returns false if the wait gave up.
+template <int MODE>
+__device__ __forceinline__ bool promote_block(Smem& s, float (&acc)[128], uint32_t lane_addr,
+                                              int hf, int lane, uint32_t pc, float sa, float s0,
+                                              float s1, volatile int* abort_flag) {
+  const int buf = pc & 1;
+  if (!mbar_wait(&s.pfull[buf], (pc >> 1) & 1u, abort_flag)) return false;
+  tc_fence_after();
+  const uint32_t taddr = lane_addr + static_cast<uint32_t>(buf * BN);
+  // Four batches of 32 columns.  The partial goes back to the MMA thread as
+  // soon as the last batch is in registers (tcgen05.wait::ld returns once
+  // the loads have completed), before that batch's FMAs.
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    float x0[16], x1[16];
+    if (MODE == GATEUP) {
+      tmem_ld16(taddr + hf * 64 + r * 16, x0);            // gate columns
+      tmem_ld16(taddr + BN / 2 + hf * 64 + r * 16, x1);   // matching up columns
+    } else {
+      tmem_ld16(taddr + hf * 128 + r * 32, x0);
+      tmem_ld16(taddr + hf * 128 + r * 32 + 16, x1);
+    }
+    tmem_ld_wait();
+    if (r == 3) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.pempty[buf]);
+    }
+    if (MODE == GATEUP) {
+      const float sg = sa * s0, su = sa * s1;
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        ffma2_bcast(acc[r * 16 + i], acc[r * 16 + i + 1], x0[i], x0[i + 1], sg);
+        ffma2_bcast(acc[64 + r * 16 + i], acc[64 + r * 16 + i + 1], x1[i], x1[i + 1], su);
+      }
+    } else {
+      const float sc = sa * s0;
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        ffma2_bcast(acc[r * 32 + i], acc[r * 32 + i + 1], x0[i], x0[i + 1], sc);
+        ffma2_bcast(acc[r * 32 + 16 + i], acc[r * 32 + 16 + i + 1], x1[i], x1[i + 1], sc);
+      }
+    }
+  }
+  return true;
 }
 
 template <int MODE>
@@ -212,7 +301,8 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
     for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&s.pfull[i], 1); mbar_init(&s.pempty[i], EPI_WARPS); }
     mbar_init(&s.xch, EPI_WARPS * 32);
-    mbar_init(&s.done, 1);
+    mbar_init(&s.done[0], 1);
+    mbar_init(&s.done[1], 1);
     s.abort = 0;
     fence_mbarrier_init();
   }
@@ -227,6 +317,8 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
   const uint32_t tmem_base = s.tmem_base;
   const int total = s.gstart[s.n_groups];
 
+  if (warp < EPI_WARP0) {
+    regs_dec<REGS_LOW>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -241,30 +333,32 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         const int a_row = tl.row0 + tl.mt * BM;
         const CUtensorMap* am = &p.a_map[tl.cls];
         const CUtensorMap* bm = &p.b_map[tl.cls];
+        // B rows of the tile: gate/up, the W1 and W3 rows of 128 h columns;
+        // down, 256 rows of W2 of the matrix that holds the current K block
+        // (the shared class walks K over its N_s matrices)
+        int by0, by1, bxk = 0;
+        if (MODE == GATEUP) {
+          const int n0 = tl.nt * (BN / 2);
+          const int base = (tl.cls == 0 ? tl.group : n0 / p.inter) * 2 * p.inter;
+          by0 = base + n0 % p.inter;
+          by1 = by0 + p.inter;
+        } else {
+          by0 = (tl.cls == 0 ? tl.group : 0) * p.d + tl.nt * BN;
+          by1 = by0 + BN / 2;
+        }
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) break;
           uint8_t* sa = ring + stage * A_BYTES;
           uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
           mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
           tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
-          int bx, by0, by1;
-          if (MODE == GATEUP) {
-            const int n0 = tl.nt * (BN / 2);
-            const int sh = n0 / p.inter, i0 = n0 % p.inter;
-            const int base = (tl.cls == 0 ? tl.group : sh) * 2 * p.inter;
-            bx = kb * BK;
-            by0 = base + i0;
-            by1 = base + p.inter + i0;
-          } else {
-            const int k0 = kb * BK;
-            const int sh = k0 / p.inter;
-            const int ex = tl.cls == 0 ? tl.group : sh;
-            bx = tl.cls == 0 ? k0 : k0 % p.inter;
-            by0 = ex * p.d + tl.nt * BN;
-            by1 = by0 + BN / 2;
-          }
+          const int bx = MODE == GATEUP ? kb * BK : bxk;
           tma_load_2d(sb, bm, &s.full[stage], bx, by0, pol_b);
           tma_load_2d(sb + B_HALF_BYTES, bm, &s.full[stage], bx, by1, pol_b);
+          if (MODE == DOWN) {
+            bxk += BK;
+            if (bxk == p.inter) { bxk = 0; by0 += p.d; by1 += p.d; }
+          }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -274,42 +368,51 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         drain_wait(&s.full[stage], phase);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     // ----------------------------------------------------------------- MMA
+    // Two issuing threads: warp 1 takes the even K blocks of the CTA's
+    // block sequence (TMEM partial 0, ring stages 0 and 2), warp 2 the odd
+    // ones (partial 1, stages 1 and 3).  Each K block is a separate
+    // accumulation into its own partial, so the two need no mutual order.
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, pc = 0;
+      const int par = warp - 1;
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(par * BN);
+      uint32_t pc = 0;   // K blocks of the CTA so far
+      uint32_t mine = 0; // K blocks of this issuer so far
       bool any = false, ok = true;
       for (int t = blockIdx.x; t < total && ok && !*abort_flag; t += gridDim.x) {
         const Tile tl = decode_tile<MODE>(p, s, t);
         const int nk = p.cls[tl.cls].k_dim / BK;
-        for (int kb = 0; kb < nk; ++kb, ++pc) {
-          const int buf = pc & 1;
-          if (!mbar_wait(&s.pempty[buf], ((pc >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        uint32_t kb0 = (pc & 1u) == static_cast<uint32_t>(par) ? 0u : 1u;
+        for (uint32_t kb = kb0; kb < static_cast<uint32_t>(nk); kb += 2, ++mine) {
+          const int stage = par + 2 * static_cast<int>(mine & 1u);
+          const uint32_t sphase = (mine >> 1) & 1u;
+          if (!mbar_wait(&s.pempty[par], (mine & 1u) ^ 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          if (!mbar_wait(&s.full[stage], phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.full[stage], sphase, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-          const uint32_t a0 = smem_u32(ring + stage * A_BYTES);
-          const uint32_t b0 = smem_u32(ring + STAGES * A_BYTES + stage * B_BYTES);
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(ring + stage * A_BYTES));
+          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(ring + STAGES * A_BYTES + stage * B_BYTES));
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            mma_fp8_ss(d_tmem, sdesc_kmajor_sw128(a0 + k * 32), sdesc_kmajor_sw128(b0 + k * 32),
-                       IDESC, k != 0 ? 1u : 0u);
+          for (int k = 0; k < BK / 32; ++k)  // +32 bytes along K = +2 in the address field
+            mma_fp8_ss(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, k != 0 ? 1u : 0u);
           any = true;
           mma_commit(&s.empty[stage]);
-          mma_commit(&s.pfull[buf]);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          mma_commit(&s.pfull[par]);
         }
+        pc += static_cast<uint32_t>(nk);
       }
       if (any) {
-        mma_commit(&s.done);
-        drain_wait(&s.done, 0);
+        mma_commit(&s.done[par]);
+        drain_wait(&s.done[par], 0);
       }
     }
+  }
   } else {
+    regs_inc<REGS_HIGH>();
     // ------------------------------------------------- promotion + epilogue
-    const int q = warp & 3;              // TMEM lane quarter of this warp
-    const int hf = (warp - 2) >> 2;      // column half
+    const int q = warp & 3;                   // TMEM lane quarter of this warp
+    const int hf = (warp - EPI_WARP0) >> 2;   // column half
     const int r_in_tile = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t pc = 0;
@@ -321,53 +424,35 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
       const int m = tl.mt * BM + r_in_tile;
       const bool valid = m < tl.rows;
       const size_t grow = static_cast<size_t>(tl.row0) + (valid ? m : 0);
-      const float* sa_row = cd.a_scales + grow * nk;
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+      ScaleCursor<MODE> sc;
+      sc.init(p, tl, hf, valid, grow);
+      // two-slot register ring of scales, loaded two K blocks ahead
+      float sa0, w00, w10, sa1 = 0.f, w01 = 0.f, w11 = 0.f;
+      sc.next(sa0, w00, w10);
+      if (nk > 1) sc.next(sa1, w01, w11);
       bool ok = true;
-      float sa_next = valid ? __ldg(sa_row) : 0.f;
-      float s0n, s1n;
-      weight_scales<MODE>(p, tl, hf, 0, s0n, s1n);
-      for (int kb = 0; kb < nk; ++kb, ++pc) {
-        const float sa = sa_next;
-        const float s0 = s0n, s1 = s1n;
+      for (int kb = 0; kb < nk; kb += 2) {
+        {
+          const float a_ = sa0, b_ = w00, c_ = w10;
+          if (kb + 2 < nk) sc.next(sa0, w00, w10);
+          if (!promote_block<MODE>(s, acc, lane_addr, hf, lane, pc, a_, b_, c_, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ++pc;
+        }
         if (kb + 1 < nk) {
-          sa_next = valid ? __ldg(sa_row + kb + 1) : 0.f;
-          weight_scales<MODE>(p, tl, hf, kb + 1, s0n, s1n);
-        }
-        const int buf = pc & 1;
-        if (!mbar_wait(&s.pfull[buf], (pc >> 1) & 1u, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t taddr = lane_addr + static_cast<uint32_t>(buf * BN);
-        if (MODE == GATEUP) {
-          const float sg = sa * s0, su = sa * s1;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float g[8], u[8];
-            tmem_ld8(taddr + hf * 64 + j * 8, g);
-            tmem_ld8(taddr + BN / 2 + hf * 64 + j * 8, u);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              acc[j * 8 + i] = fmaf(g[i], sg, acc[j * 8 + i]);
-              acc[64 + j * 8 + i] = fmaf(u[i], su, acc[64 + j * 8 + i]);
-            }
+          const float a_ = sa1, b_ = w01, c_ = w11;
+          if (kb + 3 < nk) sc.next(sa1, w01, w11);
+          if (!promote_block<MODE>(s, acc, lane_addr, hf, lane, pc, a_, b_, c_, abort_flag)) {
+            ok = false;
+            break;
           }
-        } else {
-          const float sc = sa * s0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float v[16];
-            tmem_ld16(taddr + hf * 128 + j * 16, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(v[i], sc, acc[j * 16 + i]);
-          }
+          ++pc;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.pempty[buf]);
       }
       if (!ok) break;
 
