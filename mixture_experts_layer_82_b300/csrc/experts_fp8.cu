@@ -174,11 +174,6 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int 
   return tl;
 }
 
-__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
-  int never = 0;
-  return mbar_wait(bar, parity, &never);
-}
-
 // Scales of the epilogue thread's row and columns, K block after K block.
 // Activation: sa[row, kb] (0 for a row past the segment).  Gate/up: the
 // W1 block and the matching W3 block of the tile's 128 h columns.  Down:
@@ -241,11 +236,13 @@ struct ScaleCursor {
 
 // Promotion of one K block: waits for its TMEM partial, adds
 // partial * sa * sw to the fp32 accumulators and hands the partial back to
-// the MMA thread.  Returns false if the wait gave up.
+// the MMA thread.  lane_addr: the warp's TMEM lanes at its first column
+// (gate/up: the half's first gate column; down: the half's first column).
+// Returns false if the wait gave up.
 template <int MODE>
 __device__ __forceinline__ bool promote_block(Smem& s, float (&acc)[128], uint32_t lane_addr,
-                                              int hf, int lane, uint32_t pc, float sa, float s0,
-                                              float s1, volatile int* abort_flag) {
+                                              int lane, uint32_t pc, float sa, float s0, float s1,
+                                              volatile int* abort_flag) {
   const int buf = pc & 1;
   if (!mbar_wait(&s.pfull[buf], (pc >> 1) & 1u, abort_flag)) return false;
   tc_fence_after();
@@ -257,11 +254,11 @@ __device__ __forceinline__ bool promote_block(Smem& s, float (&acc)[128], uint32
   for (int r = 0; r < 4; ++r) {
     float x0[16], x1[16];
     if (MODE == GATEUP) {
-      tmem_ld16(taddr + hf * 64 + r * 16, x0);            // gate columns
-      tmem_ld16(taddr + BN / 2 + hf * 64 + r * 16, x1);   // matching up columns
+      tmem_ld16(taddr + r * 16, x0);            // gate columns
+      tmem_ld16(taddr + BN / 2 + r * 16, x1);   // matching up columns
     } else {
-      tmem_ld16(taddr + hf * 128 + r * 32, x0);
-      tmem_ld16(taddr + hf * 128 + r * 32 + 16, x1);
+      tmem_ld16(taddr + r * 32, x0);
+      tmem_ld16(taddr + r * 32 + 16, x1);
     }
     tmem_ld_wait();
     if (r == 3) {
@@ -365,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
       }
       for (int i = 0; i < STAGES && i < issued; ++i) {
         if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
-        drain_wait(&s.full[stage], phase);
+        mbar_wait_drain(&s.full[stage], phase);
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -404,31 +401,40 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
       }
       if (any) {
         mma_commit(&s.done[par]);
-        drain_wait(&s.done[par], 0);
+        mbar_wait_drain(&s.done[par], 0);
       }
     }
   }
   } else {
     regs_inc<REGS_HIGH>();
     // ------------------------------------------------- promotion + epilogue
+    // The TMEM base and the tile count are read from shared memory again
+    // here, so that no value computed before the role split (where the
+    // producer/MMA warpgroup's 56-register budget applies) is live in this
+    // warpgroup's loops.
+    const uint32_t tmem_base_e = *reinterpret_cast<volatile uint32_t*>(&s.tmem_base);
+    const int total_e = reinterpret_cast<volatile int*>(s.gstart)[s.n_groups];
     const int q = warp & 3;                   // TMEM lane quarter of this warp
     const int hf = (warp - EPI_WARP0) >> 2;   // column half
-    const int r_in_tile = q * 32 + lane;
-    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t lane_addr = tmem_base_e + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(hf * (MODE == GATEUP ? 64 : 128));
     uint32_t pc = 0;
-    int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const Tile tl = decode_tile<MODE>(p, s, t);
-      const ClassDesc& cd = p.cls[tl.cls];
-      const int nk = cd.k_dim / BK;
-      const int m = tl.mt * BM + r_in_tile;
-      const bool valid = m < tl.rows;
-      const size_t grow = static_cast<size_t>(tl.row0) + (valid ? m : 0);
+    for (int t = blockIdx.x; t < total_e; t += gridDim.x) {
+      const int r_in_tile = q * 32 + lane;
+      // Only the scale cursor and the K count stay live through the K loop;
+      // the tile is decoded again for the store (register pressure).
+      int nk;
+      ScaleCursor<MODE> sc;
+      {
+        const Tile tl = decode_tile<MODE>(p, s, t);
+        nk = p.cls[tl.cls].k_dim / BK;
+        const int m = tl.mt * BM + r_in_tile;
+        const bool valid = m < tl.rows;
+        sc.init(p, tl, hf, valid, static_cast<size_t>(tl.row0) + (valid ? m : 0));
+      }
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-      ScaleCursor<MODE> sc;
-      sc.init(p, tl, hf, valid, grow);
       // two-slot register ring of scales, loaded two K blocks ahead
       float sa0, w00, w10, sa1 = 0.f, w01 = 0.f, w11 = 0.f;
       sc.next(sa0, w00, w10);
@@ -438,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         {
           const float a_ = sa0, b_ = w00, c_ = w10;
           if (kb + 2 < nk) sc.next(sa0, w00, w10);
-          if (!promote_block<MODE>(s, acc, lane_addr, hf, lane, pc, a_, b_, c_, abort_flag)) {
+          if (!promote_block<MODE>(s, acc, lane_addr, lane, pc, a_, b_, c_, abort_flag)) {
             ok = false;
             break;
           }
@@ -447,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         if (kb + 1 < nk) {
           const float a_ = sa1, b_ = w01, c_ = w11;
           if (kb + 3 < nk) sc.next(sa1, w01, w11);
-          if (!promote_block<MODE>(s, acc, lane_addr, hf, lane, pc, a_, b_, c_, abort_flag)) {
+          if (!promote_block<MODE>(s, acc, lane_addr, lane, pc, a_, b_, c_, abort_flag)) {
             ok = false;
             break;
           }
@@ -456,6 +462,11 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
       }
       if (!ok) break;
 
+      const Tile tl = decode_tile<MODE>(p, s, t);
+      const ClassDesc& cd = p.cls[tl.cls];
+      const int m = tl.mt * BM + r_in_tile;
+      const bool valid = m < tl.rows;
+      const size_t grow = static_cast<size_t>(tl.row0) + (valid ? m : 0);
       if (MODE == GATEUP) {
         // h = silu(a) * b, then one E4M3 scale per row and 128 h columns
         float amax = 0.f;
@@ -465,6 +476,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
           acc[i] = h;
           amax = fmaxf(amax, fabsf(h));
         }
+        const int it = (t - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x);
         const int xb = it & 1;
         s.red[xb][hf][r_in_tile] = amax;
         mbar_arrive(&s.xch);

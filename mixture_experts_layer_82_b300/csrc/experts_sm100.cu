@@ -148,12 +148,6 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int 
   return tl;
 }
 
-// Bounded wait that ignores the abort flag (used while draining).
-__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
-  int never = 0;
-  return mbar_wait(bar, parity, &never);
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) experts_bf16_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -229,7 +223,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_kernel(const __grid_c
       // Drain: wait until the last loads of every stage have landed.
       for (int i = 0; i < STAGES && i < issued; ++i) {
         if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
-        drain_wait(&s.full[stage], phase);
+        mbar_wait_drain(&s.full[stage], phase);
       }
     }
   } else if (warp == 1) {
@@ -267,7 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_kernel(const __grid_c
       // Drain: every MMA issued by this thread has completed after this.
       if (any) {
         mma_commit(&s.done);
-        drain_wait(&s.done, 0);
+        mbar_wait_drain(&s.done, 0);
       }
     }
   } else {

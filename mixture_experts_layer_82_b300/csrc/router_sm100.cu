@@ -106,8 +106,7 @@ __global__ void __launch_bounds__(THREADS, 1) router_tc_kernel(const __grid_cons
       }
       for (int i = 0; i < STAGES && i < issued; ++i) {  // drain own copies
         if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
-        int never = 0;
-        mbar_wait(&s.full[stage], phase, &never);
+        mbar_wait_drain(&s.full[stage], phase);
       }
     }
   } else if (warp == 1) {
@@ -142,8 +141,7 @@ __global__ void __launch_bounds__(THREADS, 1) router_tc_kernel(const __grid_cons
       }
       if (any) {  // drain: every MMA issued here has completed after this
         mma_commit(&s.done);
-        int never = 0;
-        mbar_wait(&s.done, 0, &never);
+        mbar_wait_drain(&s.done, 0);
       }
     }
   } else {
