@@ -25,11 +25,11 @@
 // weight tile through L2.
 //
 // Roles (384 threads = 3 warpgroups, one CTA per SM):
-//   warp 0      TMA producer: A and B tiles into a 4-stage ring (48 KB/stage)
+//   warps 0, 3  TMA producers (even / odd K blocks): A and B tiles into a
+//               4-stage ring (48 KB/stage), one TMA load each per stage
 //   warp 1      allocates 512 TMEM columns; warps 1 and 2 issue
 //               tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32), 4 per block,
 //               one thread each, for alternate K blocks
-//   warp 3      idle
 //   warps 4..11 promotion + epilogue.  Warp w reads TMEM lanes
 //               32*(w%4)..+31 (its rows); warpgroup 1 owns column half 0,
 //               warpgroup 2 half 1.  Gate/up: a half is 64 gate columns and
@@ -38,9 +38,9 @@
 //               for the 1 x 128 requantisation.  Down: a half is one
 //               128-column weight block.
 // Registers: launched at 168 per thread; warpgroup 0 gives its share down
-// to 56 and the two epilogue warpgroups take 224 each (4*32*56 +
-// 8*32*224 = 384*168), room for 128 fp32 accumulators, a 32-column batch
-// of TMEM loads and the scales, which are loaded two K blocks ahead.
+// to 40 and the two epilogue warpgroups take 232 each (4*32*40 +
+// 8*32*232 = 384*168), room for 128 fp32 accumulators, one batch of TMEM
+// loads and the scales, which are loaded two K blocks ahead (no spills).
 // Every wait is bounded; a wait that gives up sets the error word and the
 // block-wide abort flag, so all roles leave, drain their own copies in
 // flight and free TMEM.
@@ -57,11 +57,10 @@ constexpr int BM = 128, BN = 256, BK = 128;  // BK bytes = one 128-byte swizzle 
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;             // 16 KiB
 constexpr int B_BYTES = BN * BK;             // 32 KiB
-constexpr int B_HALF_BYTES = B_BYTES / 2;    // one 128-row box
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;                 // first epilogue warp (warpgroup 1)
 constexpr int THREADS = 128 + EPI_WARPS * 32;
-constexpr uint32_t REGS_LOW = 56, REGS_HIGH = 224;  // after setmaxnreg
+constexpr uint32_t REGS_LOW = 40, REGS_HIGH = 232;  // after setmaxnreg
 static_assert(4 * 32 * REGS_LOW + EPI_WARPS * 32 * REGS_HIGH <= THREADS * 168,
               "register split above the launch allocation");
 constexpr int MAX_GROUPS = 1025;             // 1024 routed experts + the shared class
@@ -247,37 +246,41 @@ __device__ __forceinline__ bool promote_block(Smem& s, float (&acc)[128], uint32
   if (!mbar_wait(&s.pfull[buf], (pc >> 1) & 1u, abort_flag)) return false;
   tc_fence_after();
   const uint32_t taddr = lane_addr + static_cast<uint32_t>(buf * BN);
-  // Four batches of 32 columns.  The partial goes back to the MMA thread as
-  // soon as the last batch is in registers (tcgen05.wait::ld returns once
-  // the loads have completed), before that batch's FMAs.
+  // Gate/up: four batches of 16 gate + 16 up columns; down: two batches of
+  // 64 columns (what the register budget allows without spilling).  The
+  // partial goes back to the MMA thread as soon as the last batch is in
+  // registers (tcgen05.wait::ld returns once the loads have completed),
+  // before that batch's FMAs.
+  constexpr int NB = MODE == GATEUP ? 4 : 2;  // batches
+  constexpr int W = 128 / (2 * NB);           // columns per load
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    float x0[16], x1[16];
+  for (int r = 0; r < NB; ++r) {
+    float x0[W], x1[W];
     if (MODE == GATEUP) {
-      tmem_ld16(taddr + r * 16, x0);            // gate columns
-      tmem_ld16(taddr + BN / 2 + r * 16, x1);   // matching up columns
+      tmem_ld_cols<W>(taddr + r * W, x0);            // gate columns
+      tmem_ld_cols<W>(taddr + BN / 2 + r * W, x1);   // matching up columns
     } else {
-      tmem_ld16(taddr + r * 32, x0);
-      tmem_ld16(taddr + r * 32 + 16, x1);
+      tmem_ld_cols<W>(taddr + r * 2 * W, x0);
+      tmem_ld_cols<W>(taddr + r * 2 * W + W, x1);
     }
     tmem_ld_wait();
-    if (r == 3) {
+    if (r == NB - 1) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.pempty[buf]);
     }
     if (MODE == GATEUP) {
       const float sg = sa * s0, su = sa * s1;
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        ffma2_bcast(acc[r * 16 + i], acc[r * 16 + i + 1], x0[i], x0[i + 1], sg);
-        ffma2_bcast(acc[64 + r * 16 + i], acc[64 + r * 16 + i + 1], x1[i], x1[i + 1], su);
+      for (int i = 0; i < W; i += 2) {
+        ffma2_bcast(acc[r * W + i], acc[r * W + i + 1], x0[i], x0[i + 1], sg);
+        ffma2_bcast(acc[64 + r * W + i], acc[64 + r * W + i + 1], x1[i], x1[i + 1], su);
       }
     } else {
       const float sc = sa * s0;
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        ffma2_bcast(acc[r * 32 + i], acc[r * 32 + i + 1], x0[i], x0[i + 1], sc);
-        ffma2_bcast(acc[r * 32 + 16 + i], acc[r * 32 + 16 + i + 1], x1[i], x1[i + 1], sc);
+      for (int i = 0; i < W; i += 2) {
+        ffma2_bcast(acc[r * 2 * W + i], acc[r * 2 * W + i + 1], x0[i], x0[i + 1], sc);
+        ffma2_bcast(acc[r * 2 * W + W + i], acc[r * 2 * W + W + i + 1], x1[i], x1[i + 1], sc);
       }
     }
   }
@@ -316,53 +319,59 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
 
   if (warp < EPI_WARP0) {
     regs_dec<REGS_LOW>();
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 3) {
+    // ----------------------------------------------------------- producers
+    // Two threads fill the ring: warp 0 the even K blocks of the CTA's block
+    // sequence (ring slots 0 and 2), warp 3 the odd ones (slots 1 and 3).
+    // A stage is two TMA loads: the A rows and the whole 256-row B tile.
     if (lane == 0) {
+      const uint32_t par = warp == 0 ? 0u : 1u;
       const uint64_t pol_a = l2_policy_evict_last();
       const uint64_t pol_b = l2_policy_evict_normal();
-      uint32_t stage = 0, phase = 0;
-      int issued = 0;
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      uint32_t g = 0;     // K blocks of the CTA so far
+      uint32_t mine = 0;  // K blocks issued by this thread
+      bool stop = false;
+      for (int t = blockIdx.x; t < total && !stop && !*abort_flag; t += gridDim.x) {
         const Tile tl = decode_tile<MODE>(p, s, t);
-        const ClassDesc& cd = p.cls[tl.cls];
-        const int nk = cd.k_dim / BK;
+        const int nk = p.cls[tl.cls].k_dim / BK;
         const int a_row = tl.row0 + tl.mt * BM;
         const CUtensorMap* am = &p.a_map[tl.cls];
         const CUtensorMap* bm = &p.b_map[tl.cls];
-        // B rows of the tile: gate/up, the W1 and W3 rows of 128 h columns;
-        // down, 256 rows of W2 of the matrix that holds the current K block
-        // (the shared class walks K over its N_s matrices)
-        int by0, by1, bxk = 0;
+        // B coordinates.  Gate/up: (k, i0, 0, matrix) in the [n][2][I][d]
+        // view, i.e. 128 W1 rows and the matching 128 W3 rows.  Down:
+        // (k inside the matrix, first row) in the [n * d, I] view; the shared
+        // class walks K over its N_s matrices.
+        int bmat = 0, bi = 0, bxk = 0, brow = 0;
         if (MODE == GATEUP) {
           const int n0 = tl.nt * (BN / 2);
-          const int base = (tl.cls == 0 ? tl.group : n0 / p.inter) * 2 * p.inter;
-          by0 = base + n0 % p.inter;
-          by1 = by0 + p.inter;
+          bmat = tl.cls == 0 ? tl.group : n0 / p.inter;
+          bi = n0 % p.inter;
         } else {
-          by0 = (tl.cls == 0 ? tl.group : 0) * p.d + tl.nt * BN;
-          by1 = by0 + BN / 2;
+          brow = (tl.cls == 0 ? tl.group : 0) * p.d + tl.nt * BN;
         }
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) break;
-          uint8_t* sa = ring + stage * A_BYTES;
-          uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
-          mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
-          tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
-          const int bx = MODE == GATEUP ? kb * BK : bxk;
-          tma_load_2d(sb, bm, &s.full[stage], bx, by0, pol_b);
-          tma_load_2d(sb + B_HALF_BYTES, bm, &s.full[stage], bx, by1, pol_b);
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          if ((g & 1u) == par) {
+            const int stage = static_cast<int>(par + 2 * (mine & 1u));
+            const uint32_t sphase = (mine >> 1) & 1u;
+            if (!mbar_wait(&s.empty[stage], sphase ^ 1u, abort_flag)) { stop = true; break; }
+            uint8_t* sa = ring + stage * A_BYTES;
+            uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
+            mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
+            if (MODE == GATEUP) tma_load_4d(sb, bm, &s.full[stage], kb * BK, bi, 0, bmat, pol_b);
+            else tma_load_2d(sb, bm, &s.full[stage], bxk, brow, pol_b);
+            tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
+            ++mine;
+          }
           if (MODE == DOWN) {
             bxk += BK;
-            if (bxk == p.inter) { bxk = 0; by0 += p.d; by1 += p.d; }
+            if (bxk == p.inter) { bxk = 0; brow += p.d; }
           }
-          ++issued;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      for (int i = 0; i < STAGES && i < issued; ++i) {
-        if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
-        mbar_wait_drain(&s.full[stage], phase);
+      // Drain: wait until this thread's last loads (one per slot) have landed.
+      for (uint32_t i = 0; i < 2 && i < mine; ++i) {
+        const uint32_t j = mine - 1 - i;
+        mbar_wait_drain(&s.full[par + 2 * (j & 1u)], (j >> 1) & 1u);
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -562,17 +571,11 @@ cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t st) {
   g.inter = I; g.d = c.d;
   CUresult r = encode_tensor_map_2d(&g.a_map[0], U8, const_cast<void*>(a.x_perm), c.d, tk,
                                     static_cast<uint64_t>(c.d), BK, BM, SW);
-  if (r == CUDA_SUCCESS)
-    r = encode_tensor_map_2d(&g.b_map[0], U8, const_cast<void*>(a.w13), c.d,
-                             static_cast<uint64_t>(c.E) * 2 * I, static_cast<uint64_t>(c.d), BK,
-                             BN / 2, SW);
+  if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[0], U8, a.w13, c.E, I, c.d, 1, BK);
   if (r == CUDA_SUCCESS && has_shared) {
     r = encode_tensor_map_2d(&g.a_map[1], U8, const_cast<void*>(a.x), c.d, c.T,
                              static_cast<uint64_t>(c.d), BK, BM, SW);
-    if (r == CUDA_SUCCESS)
-      r = encode_tensor_map_2d(&g.b_map[1], U8, const_cast<void*>(a.ws13), c.d,
-                               static_cast<uint64_t>(Ns) * 2 * I, static_cast<uint64_t>(c.d), BK,
-                               BN / 2, SW);
+    if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[1], U8, a.ws13, Ns, I, c.d, 1, BK);
   } else {
     g.a_map[1] = g.a_map[0];
     g.b_map[1] = g.b_map[0];
@@ -590,14 +593,14 @@ cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t st) {
   if (r == CUDA_SUCCESS)
     r = encode_tensor_map_2d(&dn.b_map[0], U8, const_cast<void*>(a.w2), I,
                              static_cast<uint64_t>(c.E) * c.d, static_cast<uint64_t>(I), BK,
-                             BN / 2, SW);
+                             BN, SW);
   if (r == CUDA_SUCCESS && has_shared) {
     r = encode_tensor_map_2d(&dn.a_map[1], U8, h_shared, static_cast<uint64_t>(Ns) * I, c.T,
                              static_cast<uint64_t>(Ns) * I, BK, BM, SW);
     if (r == CUDA_SUCCESS)
       r = encode_tensor_map_2d(&dn.b_map[1], U8, const_cast<void*>(a.ws2), I,
                                static_cast<uint64_t>(Ns) * c.d, static_cast<uint64_t>(I), BK,
-                               BN / 2, SW);
+                               BN, SW);
   } else {
     dn.a_map[1] = dn.a_map[0];
     dn.b_map[1] = dn.b_map[0];

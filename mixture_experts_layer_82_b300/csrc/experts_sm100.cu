@@ -16,8 +16,9 @@
 // i, i + grid, ...; inside a group the M tile varies fastest, so the CTAs
 // running at the same time share each weight tile through L2.
 //
-// Roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer: A and B tiles into a 4-stage shared-memory ring
+// Roles (224 threads, one CTA per SM):
+//   warps 0, 6  TMA producers (even / odd stages): A and B tiles into a
+//               4-stage shared-memory ring, one TMA load each per stage
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, N=256,
 //               K=16) into one of two 256-column fp32 accumulators
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM
@@ -39,8 +40,8 @@ constexpr int BM = 128, BN = 256, BK = 64;  // BK * 2 bytes = one 128-byte swizz
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;         // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;         // 32 KiB
-constexpr int B_HALF_BYTES = B_BYTES / 2;    // one 128-row box
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;
+constexpr int PRODUCER2 = 6;                 // warp of the second producer
 constexpr int MAX_GROUPS = 1025;             // 1024 routed experts + the shared class
 constexpr uint32_t TMEM_COLS = 512;          // two 256-column accumulators
 constexpr uint32_t IDESC = idesc_f32acc(1, 1, BM, BN);
@@ -176,54 +177,59 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_kernel(const __grid_c
   const uint32_t tmem_base = s.tmem_base;
   const int total = s.gstart[s.n_groups];
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == PRODUCER2) {
+    // ----------------------------------------------------------- producers
+    // Two threads fill the ring: warp 0 the even stages of the CTA's stage
+    // sequence (ring slots 0 and 2), warp 6 the odd ones (slots 1 and 3).
+    // A stage is two TMA loads: the A rows and the whole 256-row B tile.
     if (lane == 0) {
+      const uint32_t par = warp == 0 ? 0u : 1u;
       const uint64_t pol_a = l2_policy_evict_last();
       const uint64_t pol_b = l2_policy_evict_normal();
-      uint32_t stage = 0, phase = 0;
-      int issued = 0;
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      uint32_t g = 0;     // stages of the CTA so far
+      uint32_t mine = 0;  // stages issued by this thread
+      bool stop = false;
+      for (int t = blockIdx.x; t < total && !stop && !*abort_flag; t += gridDim.x) {
         const Tile tl = decode_tile<MODE>(p, s, t);
-        const ClassDesc& cd = p.cls[tl.cls];
-        const int nk = cd.k_dim / BK;
+        const int nk = p.cls[tl.cls].k_dim / BK;
         const int a_row = tl.row0 + tl.mt * BM;
         const CUtensorMap* am = &p.a_map[tl.cls];
         const CUtensorMap* bm = &p.b_map[tl.cls];
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) break;
-          uint8_t* sa = ring + stage * A_BYTES;
-          uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
-          mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
-          tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
-          int bx, by0, by1;
-          if (MODE == GATEUP) {
-            // 128 h columns starting at n0: W1 rows and the matching W3 rows
-            const int n0 = tl.nt * (BN / 2);
-            const int sh = n0 / p.inter, i0 = n0 % p.inter;
-            const int base = (tl.cls == 0 ? tl.group : sh) * 2 * p.inter;
-            bx = kb * BK;
-            by0 = base + i0;
-            by1 = base + p.inter + i0;
-          } else {
-            // 256 output columns of d; K block kb of expert-local index
-            const int k0 = kb * BK;
-            const int sh = k0 / p.inter;
-            const int ex = tl.cls == 0 ? tl.group : sh;
-            bx = tl.cls == 0 ? k0 : k0 % p.inter;
-            by0 = ex * p.d + tl.nt * BN;
-            by1 = by0 + BN / 2;
+        // B coordinates.  Gate/up: (k, i0, 0, matrix) in the [n][2][I][d]
+        // view, i.e. 128 W1 rows and the matching 128 W3 rows.  Down:
+        // (k inside the matrix, first row) in the [n * d, I] view; the shared
+        // class walks K over its N_s matrices.
+        int bmat = 0, bi = 0, bxk = 0, brow = 0;
+        if (MODE == GATEUP) {
+          const int n0 = tl.nt * (BN / 2);
+          bmat = tl.cls == 0 ? tl.group : n0 / p.inter;
+          bi = n0 % p.inter;
+        } else {
+          brow = (tl.cls == 0 ? tl.group : 0) * p.d + tl.nt * BN;
+        }
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          if ((g & 1u) == par) {
+            const int stage = static_cast<int>(par + 2 * (mine & 1u));
+            const uint32_t sphase = (mine >> 1) & 1u;
+            if (!mbar_wait(&s.empty[stage], sphase ^ 1u, abort_flag)) { stop = true; break; }
+            uint8_t* sa = ring + stage * A_BYTES;
+            uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
+            mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
+            if (MODE == GATEUP) tma_load_4d(sb, bm, &s.full[stage], kb * BK, bi, 0, bmat, pol_b);
+            else tma_load_2d(sb, bm, &s.full[stage], bxk, brow, pol_b);
+            tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
+            ++mine;
           }
-          tma_load_2d(sb, bm, &s.full[stage], bx, by0, pol_b);
-          tma_load_2d(sb + B_HALF_BYTES, bm, &s.full[stage], bx, by1, pol_b);
-          ++issued;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (MODE == DOWN) {
+            bxk += BK;
+            if (bxk == p.inter) { bxk = 0; brow += p.d; }
+          }
         }
       }
-      // Drain: wait until the last loads of every stage have landed.
-      for (int i = 0; i < STAGES && i < issued; ++i) {
-        if (stage == 0) { stage = STAGES - 1; phase ^= 1u; } else { --stage; }
-        mbar_wait_drain(&s.full[stage], phase);
+      // Drain: wait until this thread's last loads (one per slot) have landed.
+      for (uint32_t i = 0; i < 2 && i < mine; ++i) {
+        const uint32_t j = mine - 1 - i;
+        mbar_wait_drain(&s.full[par + 2 * (j & 1u)], (j >> 1) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -391,17 +397,11 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
   g.inter = I; g.d = c.d;
   CUresult r = encode_tensor_map_2d(&g.a_map[0], BF, const_cast<void*>(a.x_perm), c.d, tk,
                                     static_cast<uint64_t>(c.d) * 2, BK, BM, SW);
-  if (r == CUDA_SUCCESS)
-    r = encode_tensor_map_2d(&g.b_map[0], BF, const_cast<void*>(a.w13), c.d,
-                             static_cast<uint64_t>(c.E) * 2 * I, static_cast<uint64_t>(c.d) * 2,
-                             BK, BN / 2, SW);
+  if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[0], BF, a.w13, c.E, I, c.d, 2, BK);
   if (r == CUDA_SUCCESS && has_shared) {
     r = encode_tensor_map_2d(&g.a_map[1], BF, const_cast<void*>(a.x), c.d, c.T,
                              static_cast<uint64_t>(c.d) * 2, BK, BM, SW);
-    if (r == CUDA_SUCCESS)
-      r = encode_tensor_map_2d(&g.b_map[1], BF, const_cast<void*>(a.ws13), c.d,
-                               static_cast<uint64_t>(Ns) * 2 * I, static_cast<uint64_t>(c.d) * 2,
-                               BK, BN / 2, SW);
+    if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[1], BF, a.ws13, Ns, I, c.d, 2, BK);
   } else {
     g.a_map[1] = g.a_map[0];
     g.b_map[1] = g.b_map[0];
@@ -419,14 +419,14 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
   if (r == CUDA_SUCCESS)
     r = encode_tensor_map_2d(&dn.b_map[0], BF, const_cast<void*>(a.w2), I,
                              static_cast<uint64_t>(c.E) * c.d, static_cast<uint64_t>(I) * 2, BK,
-                             BN / 2, SW);
+                             BN, SW);
   if (r == CUDA_SUCCESS && has_shared) {
     r = encode_tensor_map_2d(&dn.a_map[1], BF, h_shared, static_cast<uint64_t>(Ns) * I, c.T,
                              static_cast<uint64_t>(Ns) * I * 2, BK, BM, SW);
     if (r == CUDA_SUCCESS)
       r = encode_tensor_map_2d(&dn.b_map[1], BF, const_cast<void*>(a.ws2), I,
                                static_cast<uint64_t>(Ns) * c.d, static_cast<uint64_t>(I) * 2, BK,
-                               BN / 2, SW);
+                               BN, SW);
   } else {
     dn.a_map[1] = dn.a_map[0];
     dn.b_map[1] = dn.b_map[0];

@@ -89,5 +89,15 @@ CUresult encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, void* base
                               uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
                               uint32_t box_inner, uint32_t box_outer,
                               CUtensorMapSwizzle swizzle);
+// Rank-n map: dims and box innermost first; strides_bytes[i] is the stride
+// of dimension i + 1.
+CUresult encode_tensor_map_nd(CUtensorMap* m, CUtensorMapDataType dt, void* base, int rank,
+                              const uint64_t* dims, const uint64_t* strides_bytes,
+                              const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+// The gate/up weights [n, 2I, d] seen as [n][2][I][d]: one box of
+// box_k x 128 x 2 x 1 is 128 W1 rows followed by the matching 128 W3 rows.
+CUresult encode_gate_up_map(CUtensorMap* m, CUtensorMapDataType dt, const void* w13, int n,
+                            int inter, int d, size_t elem_bytes, uint32_t box_k);
 
 }  // namespace moe
