@@ -142,6 +142,18 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// 5-D tiled load (coordinates innermost first), completing on the mbarrier.
+__device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* m, uint64_t* bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                            int32_t c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(c4), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -284,6 +296,20 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[W]) {
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// 32-byte global store of eight 32-bit words (the address must be 32-byte
+// aligned).
+__device__ __forceinline__ void st_global_32B(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d, uint32_t e, uint32_t f, uint32_t g,
+                                              uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a), "r"(b),
+               "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
+
+// silu(a) = a / (1 + e^-a) with the fast approximate division (at most
+// 2 ulp); used where the result is re-quantised to E4M3 right after.
+__device__ __forceinline__ float silu_fast(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 // d0 += a0 * s, d1 += a1 * s as one packed two-lane fp32 FMA (round to
 // nearest, the same result as two fmaf calls).

@@ -8,10 +8,12 @@
 //     of the reduction, the tensor-core partial sum is moved to fp32 CUDA
 //     -core registers, where the scales are applied.
 // Here the reduction is cut in 128-element K blocks (one pipeline stage).
-// The tensor cores write each block's partial product into one of two TMEM
-// partials (alternating, so the MMAs of block kb+1 run while block kb is
-// promoted); eight epilogue warps read the partial (tcgen05.ld), multiply
-// it by sa[row, kb] * sw[col block, kb] and add it to fp32 registers.
+// The tensor cores write each block's partial product, as two 128-column
+// halves, into a ring of four 128-column TMEM partials; each column half is
+// promoted by its own epilogue warpgroup, which reads the partial
+// (tcgen05.ld), multiplies it by sa[row, kb] * sw[col block, kb], adds it
+// to fp32 registers and hands it back.  The MMAs can run up to three
+// half-blocks ahead of the promotion.
 //
 // Two launches per layer, one persistent kernel each:
 //   gate/up: per 128 x 256 tile the 256 MMA columns are 128 rows of W1 and
@@ -28,12 +30,13 @@
 //   warps 0, 3  TMA producers (even / odd K blocks): A and B tiles into a
 //               4-stage ring (48 KB/stage), one TMA load each per stage
 //   warp 1      allocates 512 TMEM columns; warps 1 and 2 issue
-//               tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32), 4 per block,
-//               one thread each, for alternate K blocks
+//               tcgen05.mma.kind::f8f6f4 (M=128, N=128, K=32), 4 per block
+//               and column half, one thread each, for alternate K blocks
 //   warps 4..11 promotion + epilogue.  Warp w reads TMEM lanes
 //               32*(w%4)..+31 (its rows); warpgroup 1 owns column half 0,
 //               warpgroup 2 half 1.  Gate/up: a half is 64 gate columns and
-//               the 64 matching up columns, so SwiGLU needs no exchange;
+//               the 64 matching up columns (the B tile interleaves W1 and W3
+//               in 64-row chunks), so SwiGLU needs no exchange;
 //               the two halves of a row swap one amax through shared memory
 //               for the 1 x 128 requantisation.  Down: a half is one
 //               128-column weight block.
@@ -64,8 +67,9 @@ constexpr uint32_t REGS_LOW = 40, REGS_HIGH = 232;  // after setmaxnreg
 static_assert(4 * 32 * REGS_LOW + EPI_WARPS * 32 * REGS_HIGH <= THREADS * 168,
               "register split above the launch allocation");
 constexpr int MAX_GROUPS = 1025;             // 1024 routed experts + the shared class
-constexpr uint32_t TMEM_COLS = 512;          // two 256-column partials
-constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, BN);  // E4M3 x E4M3 -> fp32
+constexpr int PN = BN / 2;                   // columns of one TMEM partial (one column half)
+constexpr uint32_t TMEM_COLS = 512;          // four 128-column partials
+constexpr uint32_t IDESC = idesc_f32acc(0, 0, BM, PN);  // E4M3 x E4M3 -> fp32, N = 128
 
 enum { GATEUP = 0, DOWN = 1 };
 
@@ -88,13 +92,14 @@ struct Params {
   int has_shared;
   int inter;  // I
   int d;
+  int out32;  // both classes' outputs 32-byte aligned: 32-byte stores
 };
 
 struct Smem {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t pfull[2];
-  uint64_t pempty[2];
+  uint64_t pfull[4];
+  uint64_t pempty[4];
   uint64_t xch;
   uint64_t done[2];
   uint32_t tmem_base;
@@ -103,10 +108,12 @@ struct Smem {
   float red[2][2][BM];         // [tile parity][column half][row]: |h| maxima
   int gstart[MAX_GROUPS + 1];  // first tile of every group
   int mtiles[MAX_GROUPS];      // M tiles of every group
+  int off[MAX_GROUPS];         // first row of every routed group (copy of offsets[0..E])
 };
 
 constexpr size_t kRingBytes = static_cast<size_t>(STAGES) * (A_BYTES + B_BYTES);
 constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(Smem);
+static_assert(kSmemBytes <= 232448, "above the 227 KiB of shared memory a block may use");
 
 struct Tile {
   int cls;     // 0 routed, 1 shared
@@ -133,8 +140,15 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
   int sum = 0;
   for (int g = g0; g < g1; ++g) {
     int rows, cls;
-    if (g < p.E) { rows = p.offsets[g + 1] - p.offsets[g]; cls = 0; }
-    else { rows = p.T; cls = 1; }
+    if (g < p.E) {
+      const int o0 = p.offsets[g];
+      rows = p.offsets[g + 1] - o0;
+      cls = 0;
+      s.off[g] = o0;
+    } else {
+      rows = p.T;
+      cls = 1;
+    }
     const int mt = ceil_div(max(rows, 0), BM);
     s.mtiles[g] = mt;
     sum += mt * n_tiles_of<MODE>(p, cls);
@@ -151,7 +165,11 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
     const int cls = g < p.E ? 0 : 1;
     run += s.mtiles[g] * n_tiles_of<MODE>(p, cls);
   }
-  if (lane == 31) { s.gstart[G] = incl; s.n_groups = G; }
+  if (lane == 31) {
+    s.gstart[G] = incl;
+    s.n_groups = G;
+    s.off[p.E] = p.offsets[p.E];
+  }
 }
 
 template <int MODE>
@@ -168,7 +186,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int 
   const int mt_count = s.mtiles[lo];
   tl.mt = local % mt_count;
   tl.nt = local / mt_count;
-  if (tl.cls == 0) { tl.row0 = p.offsets[lo]; tl.rows = p.offsets[lo + 1] - tl.row0; }
+  if (tl.cls == 0) { tl.row0 = s.off[lo]; tl.rows = s.off[lo + 1] - tl.row0; }
   else { tl.row0 = 0; tl.rows = p.T; }
   return tl;
 }
@@ -233,22 +251,23 @@ struct ScaleCursor {
   }
 };
 
-// Promotion of one K block: waits for its TMEM partial, adds
-// partial * sa * sw to the fp32 accumulators and hands the partial back to
-// the MMA thread.  lane_addr: the warp's TMEM lanes at its first column
-// (gate/up: the half's first gate column; down: the half's first column).
-// Returns false if the wait gave up.
+// Promotion of one K block for one column half: waits for the half's TMEM
+// partial, adds partial * sa * sw to the fp32 accumulators and hands the
+// partial back to its MMA issuer.  K block pc of the CTA lives in partial
+// 2 * (pc % 2) + hf (issuer pc % 2, column half hf).  lane_addr: the warp's
+// TMEM lanes at column 0.  Returns false if the wait gave up.
 template <int MODE>
 __device__ __forceinline__ bool promote_block(Smem& s, float (&acc)[128], uint32_t lane_addr,
-                                              int lane, uint32_t pc, float sa, float s0, float s1,
-                                              volatile int* abort_flag) {
-  const int buf = pc & 1;
+                                              int hf, int lane, uint32_t pc, float sa, float s0,
+                                              float s1, volatile int* abort_flag) {
+  const int buf = 2 * static_cast<int>(pc & 1u) + hf;
   if (!mbar_wait(&s.pfull[buf], (pc >> 1) & 1u, abort_flag)) return false;
   tc_fence_after();
-  const uint32_t taddr = lane_addr + static_cast<uint32_t>(buf * BN);
-  // Gate/up: four batches of 16 gate + 16 up columns; down: two batches of
-  // 64 columns (what the register budget allows without spilling).  The
-  // partial goes back to the MMA thread as soon as the last batch is in
+  const uint32_t taddr = lane_addr + static_cast<uint32_t>(buf * PN);
+  // Gate/up: the half's 64 gate columns then its 64 up columns, in four
+  // batches of 16 + 16; down: the half's 128 columns in two batches of
+  // 32 + 32 (what the register budget allows without spilling).  The
+  // partial goes back to the MMA issuer as soon as the last batch is in
   // registers (tcgen05.wait::ld returns once the loads have completed),
   // before that batch's FMAs.
   constexpr int NB = MODE == GATEUP ? 4 : 2;  // batches
@@ -257,8 +276,8 @@ __device__ __forceinline__ bool promote_block(Smem& s, float (&acc)[128], uint32
   for (int r = 0; r < NB; ++r) {
     float x0[W], x1[W];
     if (MODE == GATEUP) {
-      tmem_ld_cols<W>(taddr + r * W, x0);            // gate columns
-      tmem_ld_cols<W>(taddr + BN / 2 + r * W, x1);   // matching up columns
+      tmem_ld_cols<W>(taddr + r * W, x0);        // gate columns
+      tmem_ld_cols<W>(taddr + 64 + r * W, x1);   // matching up columns
     } else {
       tmem_ld_cols<W>(taddr + r * 2 * W, x0);
       tmem_ld_cols<W>(taddr + r * 2 * W + W, x1);
@@ -299,7 +318,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) { tma_prefetch_desc(&p.a_map[i]); tma_prefetch_desc(&p.b_map[i]); }
     for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&s.pfull[i], 1); mbar_init(&s.pempty[i], EPI_WARPS); }
+    for (int i = 0; i < 4; ++i) { mbar_init(&s.pfull[i], 1); mbar_init(&s.pempty[i], 4); }
     mbar_init(&s.xch, EPI_WARPS * 32);
     mbar_init(&s.done[0], 1);
     mbar_init(&s.done[1], 1);
@@ -337,8 +356,10 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         const int a_row = tl.row0 + tl.mt * BM;
         const CUtensorMap* am = &p.a_map[tl.cls];
         const CUtensorMap* bm = &p.b_map[tl.cls];
-        // B coordinates.  Gate/up: (k, i0, 0, matrix) in the [n][2][I][d]
-        // view, i.e. 128 W1 rows and the matching 128 W3 rows.  Down:
+        // B coordinates.  Gate/up: (k, 0, 0, i0 / 64, matrix) in the
+        // [n][I/64][2][64][d] view: 64 W1 rows, their 64 W3 rows, the next 64
+        // W1 rows and their W3 rows, so each column half of the tile holds
+        // matching gate and up rows.  Down:
         // (k inside the matrix, first row) in the [n * d, I] view; the shared
         // class walks K over its N_s matrices.
         int bmat = 0, bi = 0, bxk = 0, brow = 0;
@@ -357,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
             uint8_t* sa = ring + stage * A_BYTES;
             uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
             mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
-            if (MODE == GATEUP) tma_load_4d(sb, bm, &s.full[stage], kb * BK, bi, 0, bmat, pol_b);
+            if (MODE == GATEUP) tma_load_5d(sb, bm, &s.full[stage], kb * BK, 0, 0, bi / 64, bmat, pol_b);
             else tma_load_2d(sb, bm, &s.full[stage], bxk, brow, pol_b);
             tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
             ++mine;
@@ -377,12 +398,12 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
   } else if (warp == 1 || warp == 2) {
     // ----------------------------------------------------------------- MMA
     // Two issuing threads: warp 1 takes the even K blocks of the CTA's
-    // block sequence (TMEM partial 0, ring stages 0 and 2), warp 2 the odd
-    // ones (partial 1, stages 1 and 3).  Each K block is a separate
-    // accumulation into its own partial, so the two need no mutual order.
+    // block sequence (TMEM partials 0 and 1, ring stages 0 and 2), warp 2
+    // the odd ones (partials 2 and 3, stages 1 and 3).  Each K block and
+    // column half is a separate accumulation into its own partial, so the
+    // two threads need no mutual order.
     if (lane == 0) {
       const int par = warp - 1;
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(par * BN);
       uint32_t pc = 0;   // K blocks of the CTA so far
       uint32_t mine = 0; // K blocks of this issuer so far
       bool any = false, ok = true;
@@ -393,18 +414,26 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         for (uint32_t kb = kb0; kb < static_cast<uint32_t>(nk); kb += 2, ++mine) {
           const int stage = par + 2 * static_cast<int>(mine & 1u);
           const uint32_t sphase = (mine >> 1) & 1u;
-          if (!mbar_wait(&s.pempty[par], (mine & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-          tc_fence_after();
           if (!mbar_wait(&s.full[stage], sphase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint64_t ad = sdesc_kmajor_sw128(smem_u32(ring + stage * A_BYTES));
-          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(ring + STAGES * A_BYTES + stage * B_BYTES));
+          // the two column halves: B rows [0, 128) and [128, 128 + 128) of the
+          // stage, each into its own partial 2 * par + h
+          for (int h = 0; h < 2; ++h) {
+            const int buf = 2 * par + h;
+            if (!mbar_wait(&s.pempty[buf], (mine & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t bd = sdesc_kmajor_sw128(
+                smem_u32(ring + STAGES * A_BYTES + stage * B_BYTES + h * (B_BYTES / 2)));
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * PN);
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)  // +32 bytes along K = +2 in the address field
-            mma_fp8_ss(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, k != 0 ? 1u : 0u);
-          any = true;
+            for (int k = 0; k < BK / 32; ++k)  // +32 bytes along K = +2 in the address field
+              mma_fp8_ss(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, k != 0 ? 1u : 0u);
+            any = true;
+            mma_commit(&s.pfull[buf]);
+          }
+          if (!ok) break;
           mma_commit(&s.empty[stage]);
-          mma_commit(&s.pfull[par]);
         }
         pc += static_cast<uint32_t>(nk);
       }
@@ -425,8 +454,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
     const int total_e = reinterpret_cast<volatile int*>(s.gstart)[s.n_groups];
     const int q = warp & 3;                   // TMEM lane quarter of this warp
     const int hf = (warp - EPI_WARP0) >> 2;   // column half
-    const uint32_t lane_addr = tmem_base_e + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(hf * (MODE == GATEUP ? 64 : 128));
+    const uint32_t lane_addr = tmem_base_e + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t pc = 0;
     for (int t = blockIdx.x; t < total_e; t += gridDim.x) {
       const int r_in_tile = q * 32 + lane;
@@ -453,7 +481,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         {
           const float a_ = sa0, b_ = w00, c_ = w10;
           if (kb + 2 < nk) sc.next(sa0, w00, w10);
-          if (!promote_block<MODE>(s, acc, lane_addr, lane, pc, a_, b_, c_, abort_flag)) {
+          if (!promote_block<MODE>(s, acc, lane_addr, hf, lane, pc, a_, b_, c_, abort_flag)) {
             ok = false;
             break;
           }
@@ -462,7 +490,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         if (kb + 1 < nk) {
           const float a_ = sa1, b_ = w01, c_ = w11;
           if (kb + 3 < nk) sc.next(sa1, w01, w11);
-          if (!promote_block<MODE>(s, acc, lane_addr, lane, pc, a_, b_, c_, abort_flag)) {
+          if (!promote_block<MODE>(s, acc, lane_addr, hf, lane, pc, a_, b_, c_, abort_flag)) {
             ok = false;
             break;
           }
@@ -481,7 +509,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const float h = silu_f(acc[i]) * acc[64 + i];
+          const float h = silu_fast(acc[i]) * acc[64 + i];
           acc[i] = h;
           amax = fmaxf(amax, fabsf(h));
         }
@@ -495,14 +523,17 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         if (valid) {
           const int n0 = tl.nt * (BN / 2);
           uint8_t* orow = static_cast<uint8_t*>(cd.out) + grow * cd.n_out + n0 + hf * 64;
+          uint32_t w[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = quant4_e4m3(acc[v * 16 + 0], acc[v * 16 + 1], acc[v * 16 + 2], acc[v * 16 + 3], scale);
-            w.y = quant4_e4m3(acc[v * 16 + 4], acc[v * 16 + 5], acc[v * 16 + 6], acc[v * 16 + 7], scale);
-            w.z = quant4_e4m3(acc[v * 16 + 8], acc[v * 16 + 9], acc[v * 16 + 10], acc[v * 16 + 11], scale);
-            w.w = quant4_e4m3(acc[v * 16 + 12], acc[v * 16 + 13], acc[v * 16 + 14], acc[v * 16 + 15], scale);
-            reinterpret_cast<uint4*>(orow)[v] = w;
+          for (int v = 0; v < 16; ++v)
+            w[v] = quant4_e4m3(acc[v * 4 + 0], acc[v * 4 + 1], acc[v * 4 + 2], acc[v * 4 + 3], scale);
+          if (p.out32) {
+            st_global_32B(orow, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            st_global_32B(orow + 32, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+          } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<uint4*>(orow)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
           }
           if (hf == 0) cd.out_scales[grow * (cd.n_out / BK) + n0 / BK] = scale;
         }
@@ -513,15 +544,16 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             if (n_base + c * 16 < cd.n_out) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
-              dst[0] = make_uint4(pack_bf16x2(acc[c * 16 + 0], acc[c * 16 + 1]),
-                                  pack_bf16x2(acc[c * 16 + 2], acc[c * 16 + 3]),
-                                  pack_bf16x2(acc[c * 16 + 4], acc[c * 16 + 5]),
-                                  pack_bf16x2(acc[c * 16 + 6], acc[c * 16 + 7]));
-              dst[1] = make_uint4(pack_bf16x2(acc[c * 16 + 8], acc[c * 16 + 9]),
-                                  pack_bf16x2(acc[c * 16 + 10], acc[c * 16 + 11]),
-                                  pack_bf16x2(acc[c * 16 + 12], acc[c * 16 + 13]),
-                                  pack_bf16x2(acc[c * 16 + 14], acc[c * 16 + 15]));
+              uint32_t w[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(acc[c * 16 + 2 * i], acc[c * 16 + 2 * i + 1]);
+              if (p.out32) {
+                st_global_32B(orow + c * 16, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              }
             }
           }
         }
@@ -571,16 +603,20 @@ cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t st) {
   g.inter = I; g.d = c.d;
   CUresult r = encode_tensor_map_2d(&g.a_map[0], U8, const_cast<void*>(a.x_perm), c.d, tk,
                                     static_cast<uint64_t>(c.d), BK, BM, SW);
-  if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[0], U8, a.w13, c.E, I, c.d, 1, BK);
+  if (r == CUDA_SUCCESS)
+    r = encode_gate_up_map_interleaved(&g.b_map[0], U8, a.w13, c.E, I, c.d, 1, BK);
   if (r == CUDA_SUCCESS && has_shared) {
     r = encode_tensor_map_2d(&g.a_map[1], U8, const_cast<void*>(a.x), c.d, c.T,
                              static_cast<uint64_t>(c.d), BK, BM, SW);
-    if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[1], U8, a.ws13, Ns, I, c.d, 1, BK);
+    if (r == CUDA_SUCCESS)
+      r = encode_gate_up_map_interleaved(&g.b_map[1], U8, a.ws13, Ns, I, c.d, 1, BK);
   } else {
     g.a_map[1] = g.a_map[0];
     g.b_map[1] = g.b_map[0];
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const auto al32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
+  g.out32 = al32(h_routed) && al32(h_shared) ? 1 : 0;
   g.cls[0] = ClassDesc{h_routed, hs_routed, a.x_perm_scales, a.w13_scales, I, c.d};
   g.cls[1] = ClassDesc{h_shared, hs_shared, has_shared ? a.x_scales : a.x_perm_scales,
                        has_shared ? a.ws13_scales : a.w13_scales, Ns * I, c.d};
@@ -606,6 +642,7 @@ cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t st) {
     dn.b_map[1] = dn.b_map[0];
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  dn.out32 = al32(a.y_perm) && (!has_shared || al32(a.y_shared)) ? 1 : 0;
   dn.cls[0] = ClassDesc{a.y_perm, nullptr, hs_routed, a.w2_scales, c.d, I};
   dn.cls[1] = ClassDesc{has_shared ? a.y_shared : a.y_perm, nullptr,
                         has_shared ? hs_shared : hs_routed,

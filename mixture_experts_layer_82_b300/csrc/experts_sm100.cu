@@ -78,10 +78,12 @@ struct Smem {
   int n_groups;
   int gstart[MAX_GROUPS + 1];  // first tile of every group
   int mtiles[MAX_GROUPS];      // M tiles of every group
+  int off[MAX_GROUPS];         // first row of every routed group (copy of offsets[0..E])
 };
 
 constexpr size_t kRingBytes = static_cast<size_t>(STAGES) * (A_BYTES + B_BYTES);
 constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(Smem);
+static_assert(kSmemBytes <= 232448, "above the 227 KiB of shared memory a block may use");
 
 struct Tile {
   int cls;      // 0 routed, 1 shared
@@ -109,8 +111,15 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
   int sum = 0;
   for (int g = g0; g < g1; ++g) {
     int rows, cls;
-    if (g < p.E) { rows = p.offsets[g + 1] - p.offsets[g]; cls = 0; }
-    else { rows = p.T; cls = 1; }
+    if (g < p.E) {
+      const int o0 = p.offsets[g];
+      rows = p.offsets[g + 1] - o0;
+      cls = 0;
+      s.off[g] = o0;
+    } else {
+      rows = p.T;
+      cls = 1;
+    }
     const int mt = ceil_div(max(rows, 0), BM);
     s.mtiles[g] = mt;
     sum += mt * n_tiles_of<MODE>(p, cls);
@@ -127,7 +136,11 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
     const int cls = g < p.E ? 0 : 1;
     run += s.mtiles[g] * n_tiles_of<MODE>(p, cls);
   }
-  if (lane == 31) { s.gstart[G] = incl; s.n_groups = G; }
+  if (lane == 31) {
+    s.gstart[G] = incl;
+    s.n_groups = G;
+    s.off[p.E] = p.offsets[p.E];
+  }
 }
 
 template <int MODE>
@@ -144,7 +157,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int 
   const int mt_count = s.mtiles[lo];
   tl.mt = local % mt_count;
   tl.nt = local / mt_count;
-  if (tl.cls == 0) { tl.row0 = p.offsets[lo]; tl.rows = p.offsets[lo + 1] - tl.row0; }
+  if (tl.cls == 0) { tl.row0 = s.off[lo]; tl.rows = s.off[lo + 1] - tl.row0; }
   else { tl.row0 = 0; tl.rows = p.T; }
   return tl;
 }

@@ -100,4 +100,11 @@ CUresult encode_tensor_map_nd(CUtensorMap* m, CUtensorMapDataType dt, void* base
 CUresult encode_gate_up_map(CUtensorMap* m, CUtensorMapDataType dt, const void* w13, int n,
                             int inter, int d, size_t elem_bytes, uint32_t box_k);
 
+// The gate/up weights [n, 2I, d] seen as [n][I/64][2][64][d]: one box of
+// box_k x 64 x 2 x 2 x 1 is 64 W1 rows, the matching 64 W3 rows, the next
+// 64 W1 rows and their 64 W3 rows (I % 128 == 0).
+CUresult encode_gate_up_map_interleaved(CUtensorMap* m, CUtensorMapDataType dt, const void* w13,
+                                        int n, int inter, int d, size_t elem_bytes,
+                                        uint32_t box_k);
+
 }  // namespace moe

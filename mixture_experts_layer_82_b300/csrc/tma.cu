@@ -47,6 +47,18 @@ CUresult encode_gate_up_map(CUtensorMap* m, CUtensorMapDataType dt, const void* 
                               CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+CUresult encode_gate_up_map_interleaved(CUtensorMap* m, CUtensorMapDataType dt, const void* w13,
+                                        int n, int inter, int d, size_t elem_bytes,
+                                        uint32_t box_k) {
+  const uint64_t dims[5] = {static_cast<uint64_t>(d), 64, 2, static_cast<uint64_t>(inter / 64),
+                            static_cast<uint64_t>(n)};
+  const uint64_t row = static_cast<uint64_t>(d) * elem_bytes;
+  const uint64_t strides[4] = {row, row * inter, row * 64, row * inter * 2};
+  const uint32_t box[5] = {box_k, 64, 2, 2, 1};
+  return encode_tensor_map_nd(m, dt, const_cast<void*>(w13), 5, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 CUresult encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t inner,
                               uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                               uint32_t box_outer, CUtensorMapSwizzle swizzle) {
