@@ -216,6 +216,44 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
+# ------------------------------------------------------------ load balance
+
+def load_stats(counts, T, K):
+    """Descriptive statistics of per-expert loads (host side)."""
+    c = np.asarray(counts, dtype=np.float64)
+    mean = T * K / len(c)
+    return {"max_over_mean": float(c.max() / mean), "cv": float(c.std() / mean),
+            "min": int(c.min()), "max": int(c.max()), "empty_experts": int((c == 0).sum())}
+
+
+def load_balance(moe, shape, L, steps):
+    """Per-expert load spread on the workload's batch before the first and
+    after `steps` sign-rule bias updates (route + bias update per step,
+    through the library; the affinities of the fixed batch are computed once
+    and passed back in)."""
+    cfg = moe.LayerCfg.from_shape(shape)
+    T, E, K = shape.T, shape.E, shape.k
+    dev = L["x"].device
+    i32 = dict(dtype=torch.int32, device=dev)
+    bufs = [torch.empty(T, K, **i32), torch.empty(T, K, dtype=torch.float32, device=dev),
+            torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(T, K, **i32),
+            torch.empty(T * K, **i32)]
+    ws = torch.empty(moe.moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    aff = torch.empty(T, E, dtype=torch.float32, device=dev)
+    bias = L["bias"].clone()
+    moe.moe_route(cfg, L["x"], L["router_w"], bias, *bufs, ws, affinity_out=aff)
+    before = load_stats(bufs[2].cpu().numpy(), T, K)
+    for i in range(steps):
+        if i:
+            moe.moe_route(cfg, None, None, bias, *bufs, ws, affinity_in=aff)
+        moe.moe_bias_update(cfg, bufs[2], bias)
+    moe.moe_route(cfg, None, None, bias, *bufs, ws, affinity_in=aff)
+    after = load_stats(bufs[2].cpu().numpy(), T, K)
+    if moe.moe_get_device_error() != 0:
+        raise RuntimeError("device error in the load-balance steps")
+    return {"bias_steps": steps, "gamma": shape.gamma, "before": before, "after": after}
+
+
 # ----------------------------------------------------------- CPU baseline
 
 def oracle_sample(shape, L, n_tokens, token0=0):
@@ -404,6 +442,8 @@ def run_ours(args, shape, world, rank, local):
         "gpu_launches": launches_per_step(shape) * K,
         "clocks": clk,
     }
+    if shape.bias_steps:
+        line["load_balance"] = load_balance(moe, shape, L, shape.bias_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs, n = oracle_sample(shape, L, args.cpu_tokens)
         line["cpu_baseline"] = {
