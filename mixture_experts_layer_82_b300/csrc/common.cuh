@@ -307,9 +307,14 @@ __device__ __forceinline__ void st_global_32B(void* p, uint32_t a, uint32_t b, u
                : "memory");
 }
 
-// silu(a) = a / (1 + e^-a) with the fast approximate division (at most
-// 2 ulp); used where the result is re-quantised to E4M3 right after.
-__device__ __forceinline__ float silu_fast(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+// silu(a) = a * sigmoid(a) = a * (1/2 + tanh(a/2) / 2), with the hardware
+// tanh approximation (one special-function operation, relative error about
+// 2^-11); used where the result is re-quantised to E4M3 right after.
+__device__ __forceinline__ float silu_fast(float a) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * a));
+  return a * fmaf(0.5f, t, 0.5f);
+}
 
 // d0 += a0 * s, d1 += a1 * s as one packed two-lane fp32 FMA (round to
 // nearest, the same result as two fmaf calls).

@@ -172,13 +172,17 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
   }
 }
 
+// Group of tile t, searching forward from group g (a CTA's tiles ascend, so
+// each role keeps its last group as the hint).
+__device__ __forceinline__ int group_from(const Smem& s, int t, int g) {
+  while (s.gstart[g + 1] <= t) ++g;
+  return g;
+}
+
 template <int MODE>
-__device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int t) {
-  int lo = 0, hi = s.n_groups;  // gstart[lo] <= t < gstart[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (s.gstart[mid] <= t) lo = mid; else hi = mid;
-  }
+__device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int t, int& g) {
+  g = group_from(s, t, g);
+  const int lo = g;
   Tile tl;
   tl.cls = lo < p.E ? 0 : 1;
   tl.group = lo;
@@ -345,13 +349,12 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
     // A stage is two TMA loads: the A rows and the whole 256-row B tile.
     if (lane == 0) {
       const uint32_t par = warp == 0 ? 0u : 1u;
-      const uint64_t pol_a = l2_policy_evict_last();
-      const uint64_t pol_b = l2_policy_evict_normal();
       uint32_t g = 0;     // K blocks of the CTA so far
       uint32_t mine = 0;  // K blocks issued by this thread
       bool stop = false;
+      int gh = 0;         // group of the last tile
       for (int t = blockIdx.x; t < total && !stop && !*abort_flag; t += gridDim.x) {
-        const Tile tl = decode_tile<MODE>(p, s, t);
+        const Tile tl = decode_tile<MODE>(p, s, t, gh);
         const int nk = p.cls[tl.cls].k_dim / BK;
         const int a_row = tl.row0 + tl.mt * BM;
         const CUtensorMap* am = &p.a_map[tl.cls];
@@ -378,9 +381,12 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
             uint8_t* sa = ring + stage * A_BYTES;
             uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
             mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
-            if (MODE == GATEUP) tma_load_5d(sb, bm, &s.full[stage], kb * BK, 0, 0, bi / 64, bmat, pol_b);
-            else tma_load_2d(sb, bm, &s.full[stage], bxk, brow, pol_b);
-            tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
+            // (the L2 policies are created at each use: registers are scarce here)
+            if (MODE == GATEUP)
+              tma_load_5d(sb, bm, &s.full[stage], kb * BK, 0, 0, bi / 64, bmat, l2_policy_evict_normal());
+            else
+              tma_load_2d(sb, bm, &s.full[stage], bxk, brow, l2_policy_evict_normal());
+            tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, l2_policy_evict_last());
             ++mine;
           }
           if (MODE == DOWN) {
@@ -407,9 +413,10 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
       uint32_t pc = 0;   // K blocks of the CTA so far
       uint32_t mine = 0; // K blocks of this issuer so far
       bool any = false, ok = true;
+      const int shared0 = s.gstart[p.E];  // first tile of the shared class
       for (int t = blockIdx.x; t < total && ok && !*abort_flag; t += gridDim.x) {
-        const Tile tl = decode_tile<MODE>(p, s, t);
-        const int nk = p.cls[tl.cls].k_dim / BK;
+        // only the tile's K length matters here: it depends on the class alone
+        const int nk = p.cls[t >= shared0 ? 1 : 0].k_dim / BK;
         uint32_t kb0 = (pc & 1u) == static_cast<uint32_t>(par) ? 0u : 1u;
         for (uint32_t kb = kb0; kb < static_cast<uint32_t>(nk); kb += 2, ++mine) {
           const int stage = par + 2 * static_cast<int>(mine & 1u);
@@ -456,6 +463,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
     const int hf = (warp - EPI_WARP0) >> 2;   // column half
     const uint32_t lane_addr = tmem_base_e + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t pc = 0;
+    int gh = 0;  // group of the last tile
     for (int t = blockIdx.x; t < total_e; t += gridDim.x) {
       const int r_in_tile = q * 32 + lane;
       // Only the scale cursor and the K count stay live through the K loop;
@@ -463,7 +471,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
       int nk;
       ScaleCursor<MODE> sc;
       {
-        const Tile tl = decode_tile<MODE>(p, s, t);
+        const Tile tl = decode_tile<MODE>(p, s, t, gh);
         nk = p.cls[tl.cls].k_dim / BK;
         const int m = tl.mt * BM + r_in_tile;
         const bool valid = m < tl.rows;
@@ -499,7 +507,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
       }
       if (!ok) break;
 
-      const Tile tl = decode_tile<MODE>(p, s, t);
+      const Tile tl = decode_tile<MODE>(p, s, t, gh);
       const ClassDesc& cd = p.cls[tl.cls];
       const int m = tl.mt * BM + r_in_tile;
       const bool valid = m < tl.rows;
@@ -520,13 +528,18 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         if (!mbar_wait(&s.xch, static_cast<uint32_t>(it) & 1u, abort_flag)) break;
         amax = fmaxf(amax, s.red[xb][hf ^ 1][r_in_tile]);
         const float scale = fp8_scale_of(amax);
+        // codes of h / scale as h * fl32(1 / scale): one correctly rounded
+        // reciprocal per row instead of 64 divisions (a code can differ from
+        // that of the exact quotient only for a value within one fp32 ulp of
+        // an E4M3 rounding midpoint)
+        const float rs = __frcp_rn(scale);
         if (valid) {
           const int n0 = tl.nt * (BN / 2);
           uint8_t* orow = static_cast<uint8_t*>(cd.out) + grow * cd.n_out + n0 + hf * 64;
           uint32_t w[16];
 #pragma unroll
           for (int v = 0; v < 16; ++v)
-            w[v] = quant4_e4m3(acc[v * 4 + 0], acc[v * 4 + 1], acc[v * 4 + 2], acc[v * 4 + 3], scale);
+            w[v] = quant4_e4m3_mul(acc[v * 4 + 0], acc[v * 4 + 1], acc[v * 4 + 2], acc[v * 4 + 3], rs);
           if (p.out32) {
             st_global_32B(orow, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
             st_global_32B(orow + 32, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);

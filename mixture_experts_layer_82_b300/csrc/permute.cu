@@ -65,6 +65,15 @@ __device__ __forceinline__ uint32_t quant4_e4m3(float a, float b, float c, float
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// E4M3 codes of a * rs ... d * rs (rs: a reciprocal scale), packed.
+__device__ __forceinline__ uint32_t quant4_e4m3_mul(float a, float b, float c, float d, float rs) {
+  const __nv_fp8x2_storage_t lo =
+      __nv_cvt_float2_to_fp8x2(make_float2(a * rs, b * rs), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi =
+      __nv_cvt_float2_to_fp8x2(make_float2(c * rs, d * rs), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
 // One warp per row; per 128-wide tile each lane holds 4 consecutive values.
 __global__ void __launch_bounds__(kRowWarps * 32) quantize_act_kernel(
     const __nv_bfloat16* __restrict__ x, int rows, int cols, uint8_t* __restrict__ q,
