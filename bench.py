@@ -92,11 +92,11 @@ def router_launches(shape):
     return 2 + (1 if splits > 1 else 0)
 
 
-def launches_per_step(shape):
+def launches_per_step(shape, gather=False):
     """Kernels one layer step launches: router product, select, scan,
-    assign; permute (quantise + permute for fp8); gate/up and down GEMMs;
-    combine; bias update."""
-    permute = 2 if shape.dtype == "fp8" else 1
+    assign; permute (quantise + permute for fp8; none when the gate/up GEMM
+    gathers its rows); gate/up and down GEMMs; combine; bias update."""
+    permute = 0 if gather else (2 if shape.dtype == "fp8" else 1)
     return router_launches(shape) + 3 + permute + 2 + 1 + 1
 
 
@@ -338,8 +338,10 @@ def run_ours(args, shape, world, rank, local):
     torch.cuda.set_device(local)
     L = make_layer(shape, dev)
     cfg = moe.LayerCfg.from_shape(shape)
+    gather = args.dispatch == "gather" and shape.dtype == "bf16"
     layer = moe.MoELayer(cfg, L["router_w"], L["bias"].clone(), L["w13"], L["w2"],
-                         L["ws13"] if shape.n_shared else None, L["ws2"] if shape.n_shared else None)
+                         L["ws13"] if shape.n_shared else None, L["ws2"] if shape.n_shared else None,
+                         gather=gather)
     x = L["x"]
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -431,6 +433,8 @@ def run_ours(args, shape, world, rank, local):
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype, "data": "synthetic",
         "config": {"workload": describe(shape), "global_batch": world * shape.T,
+                   "dispatch": "gather rows inside the gate/up GEMM" if gather
+                               else "permute kernel before the expert GEMMs",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: every step streams all expert weights "
                          f"({(3 * shape.d * shape.inter * (shape.E + shape.n_shared)) * (1 if shape.dtype == 'fp8' else 2) / 1e9:.1f} GB)"},
@@ -439,7 +443,7 @@ def run_ours(args, shape, world, rank, local):
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": out_host.numel() * out_host.element_size()},
-        "gpu_launches": launches_per_step(shape) * K,
+        "gpu_launches": launches_per_step(shape, gather) * K,
         "clocks": clk,
     }
     if shape.bias_steps:
@@ -465,6 +469,9 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dispatch", choices=["permute", "gather"], default="permute",
+                    help="bf16 kind: permute x into per-expert rows before the expert GEMMs, "
+                         "or gather the rows inside the gate/up GEMM")
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                     help="override a field of the workload's shape (a reduced case for "
                          "profiling, e.g. --set E=32 --set router=gaussian)")

@@ -197,6 +197,30 @@ moe_status_t moe_experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
                                  size_t ws_bytes, void* stream);
 
 /*
+ * moe_experts_grouped_gather - moe_experts_grouped with the permute folded
+ * into the gate/up GEMM: the routed A rows are read straight from x by
+ * token_of_row instead of from a permuted copy (the single-device dispatch
+ * of the cross-node all-to-all paragraph, done while the expert GEMM loads
+ * its operands; x_perm is never written).
+ *
+ *   x             [T, d] bf16: the layer input (routed and shared rows)
+ *   token_of_row  [T * K] from moe_route
+ *   everything else as in moe_experts_grouped (x_perm is not an argument)
+ *
+ * BF16 kind only (MOE_ERR_SHAPE otherwise).  Results are bitwise equal to
+ * moe_permute followed by moe_experts_grouped.  A token index outside
+ * [0, T) sets the error word (MOE_ERR_DEVICE) and its row is skipped.
+ */
+moe_status_t moe_experts_grouped_gather(const moe_cfg_t* cfg, const void* x,
+                                        const float* x_scales, const int32_t* token_of_row,
+                                        const int32_t* offsets, const void* w13,
+                                        const float* w13_scales, const void* w2,
+                                        const float* w2_scales, const void* ws13,
+                                        const float* ws13_scales, const void* ws2,
+                                        const float* ws2_scales, void* y_perm, void* y_shared,
+                                        void* ws, size_t ws_bytes, void* stream);
+
+/*
  * moe_combine - gate-weighted un-permute:
  *   out[t] = y_shared[t] + sum_{k < K} topk_w[t, k] * y_perm[row_of_slot[t, k]]
  * summed in fp32 in exactly that order (DeepSeekMoE paragraph).

@@ -39,7 +39,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR
 EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_bytes",
             "moe_route", "moe_permute", "moe_experts_grouped", "moe_combine",
             "moe_bias_update", "moe_quantize_weights_fp8", "moe_get_device_error",
-            "moe_route_static_scratch")
+            "moe_route_static_scratch", "moe_experts_grouped_gather")
 
 
 class MoeCfg(ctypes.Structure):
@@ -74,6 +74,8 @@ _lib.moe_permute.restype = ctypes.c_int
 _lib.moe_permute.argtypes = [_CFG] + [_P] * 6 + [_P]
 _lib.moe_experts_grouped.restype = ctypes.c_int
 _lib.moe_experts_grouped.argtypes = [_CFG] + [_P] * 15 + [_P, ctypes.c_size_t, _P]
+_lib.moe_experts_grouped_gather.restype = ctypes.c_int
+_lib.moe_experts_grouped_gather.argtypes = [_CFG] + [_P] * 14 + [_P, ctypes.c_size_t, _P]
 _lib.moe_combine.restype = ctypes.c_int
 _lib.moe_combine.argtypes = [_CFG] + [_P] * 5 + [_P]
 _lib.moe_bias_update.restype = ctypes.c_int
@@ -218,6 +220,26 @@ def moe_experts_grouped(cfg, x_perm, x, offsets, w13, w2, ws13, ws2, y_perm, y_s
         _ptr(x, "x", _X + _F8, allow_none=True),
         _ptr(x_scales, "x_scales", torch.float32, allow_none=True),
         _ptr(offsets, "offsets", torch.int32), _ptr(w13, "w13", _X + _F8),
+        _ptr(w13_scales, "w13_scales", torch.float32, allow_none=True),
+        _ptr(w2, "w2", _X + _F8), _ptr(w2_scales, "w2_scales", torch.float32, allow_none=True),
+        _ptr(ws13, "ws13", _X + _F8, allow_none=True),
+        _ptr(ws13_scales, "ws13_scales", torch.float32, allow_none=True),
+        _ptr(ws2, "ws2", _X + _F8, allow_none=True),
+        _ptr(ws2_scales, "ws2_scales", torch.float32, allow_none=True),
+        _ptr(y_perm, "y_perm", _X), _ptr(y_shared, "y_shared", _X, allow_none=True),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_experts_grouped_gather(cfg, x, token_of_row, offsets, w13, w2, ws13, ws2, y_perm,
+                               y_shared, ws, x_scales=None, w13_scales=None, w2_scales=None,
+                               ws13_scales=None, ws2_scales=None, stream=None):
+    """moe_experts_grouped with the permute folded into the gate/up GEMM
+    (routed A rows read from x by token_of_row)."""
+    _check("moe_experts_grouped_gather", _lib.moe_experts_grouped_gather(
+        _cfg(cfg), _ptr(x, "x", _X + _F8),
+        _ptr(x_scales, "x_scales", torch.float32, allow_none=True),
+        _ptr(token_of_row, "token_of_row", torch.int32), _ptr(offsets, "offsets", torch.int32),
+        _ptr(w13, "w13", _X + _F8),
         _ptr(w13_scales, "w13_scales", torch.float32, allow_none=True),
         _ptr(w2, "w2", _X + _F8), _ptr(w2_scales, "w2_scales", torch.float32, allow_none=True),
         _ptr(ws13, "ws13", _X + _F8, allow_none=True),

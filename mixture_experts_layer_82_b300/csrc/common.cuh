@@ -154,6 +154,23 @@ __device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only, with a cache policy).
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_dst),
+               "l"(src), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Offset of 16-byte chunk c of row r in a tile stored with the 128-byte
+// swizzle (rows of 128 bytes, 8-row atoms of 1024 bytes): the layout TMA
+// writes for CU_TENSOR_MAP_SWIZZLE_128B and the MMA descriptors read.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

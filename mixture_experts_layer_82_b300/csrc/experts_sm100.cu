@@ -42,6 +42,8 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;         // 32 KiB
 constexpr int THREADS = 224;
 constexpr int PRODUCER2 = 6;                 // warp of the second producer
+constexpr int GATHER_WARP0 = 7;              // gathering gate/up: warps 7..10, one per ring slot
+constexpr int THREADS_GATHER = THREADS + STAGES * 32;
 constexpr int MAX_GROUPS = 1025;             // 1024 routed experts + the shared class
 constexpr uint32_t TMEM_COLS = 512;          // two 256-column accumulators
 constexpr uint32_t IDESC = idesc_f32acc(1, 1, BM, BN);
@@ -65,6 +67,9 @@ struct Params {
   int has_shared;
   int inter;  // I: intermediate size of one expert
   int d;
+  // gathering gate/up only: routed A rows are x[token_of_row[r]]
+  const int32_t* token_of_row;
+  const __nv_bfloat16* x_rows;  // [T, d]
 };
 
 struct Smem {
@@ -79,6 +84,7 @@ struct Smem {
   int gstart[MAX_GROUPS + 1];  // first tile of every group
   int mtiles[MAX_GROUPS];      // M tiles of every group
   int off[MAX_GROUPS];         // first row of every routed group (copy of offsets[0..E])
+  int gather_tok[STAGES][BM];  // gathering gate/up: x row of each tile row, per ring slot
 };
 
 constexpr size_t kRingBytes = static_cast<size_t>(STAGES) * (A_BYTES + B_BYTES);
@@ -162,8 +168,9 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int 
   return tl;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1) experts_bf16_kernel(const __grid_constant__ Params p) {
+template <int MODE, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
+    experts_bf16_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -173,7 +180,9 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) { tma_prefetch_desc(&p.a_map[i]); tma_prefetch_desc(&p.b_map[i]); }
-    for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
+    // a stage is full once the producer's TMA bytes have landed and, when
+    // gathering, the slot's gather warp has arrived
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], GATHER ? 2 : 1); mbar_init(&s.empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&s.tfull[i], 1); mbar_init(&s.tempty[i], 4); }
     mbar_init(&s.done, 1);
     s.abort = 0;
@@ -227,10 +236,12 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_kernel(const __grid_c
             if (!mbar_wait(&s.empty[stage], sphase ^ 1u, abort_flag)) { stop = true; break; }
             uint8_t* sa = ring + stage * A_BYTES;
             uint8_t* sb = ring + STAGES * A_BYTES + stage * B_BYTES;
-            mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
+            // gathering: the routed A rows come from the slot's gather warp
+            const bool a_by_tma = !GATHER || tl.cls != 0;
+            mbar_arrive_expect_tx(&s.full[stage], (a_by_tma ? A_BYTES : 0) + B_BYTES);
             if (MODE == GATEUP) tma_load_4d(sb, bm, &s.full[stage], kb * BK, bi, 0, bmat, pol_b);
             else tma_load_2d(sb, bm, &s.full[stage], bxk, brow, pol_b);
-            tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
+            if (a_by_tma) tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
             ++mine;
           }
           if (MODE == DOWN) {
@@ -245,6 +256,61 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_kernel(const __grid_c
         mbar_wait_drain(&s.full[par + 2 * (j & 1u)], (j >> 1) & 1u);
       }
     }
+  } else if (GATHER && warp >= GATHER_WARP0) {
+    // ------------------------------------------------------- gather warps
+    // Warp GATHER_WARP0 + j fills the A rows of ring slot j (stages
+    // j, j + 4, ...) for routed tiles: row r of the tile is row
+    // token_of_row[segment row] of x (kept per tile in a warp-private
+    // shared table), copied in 16-byte pieces with cp.async, eight lanes
+    // per 128-byte row, into the 128-byte-swizzled layout the MMA
+    // descriptors read (the layout TMA writes).  Each lane waits for its own copies, makes
+    // them visible to the async proxy, and lane 0 arrives on the slot's
+    // full barrier.  Rows past the segment are not written (their MMA rows
+    // are never stored).
+    const int slot = warp - GATHER_WARP0;
+    const uint64_t pol_x = l2_policy_evict_last();
+    int* rowsrc = s.gather_tok[slot];  // x row of each tile row (-1: none)
+    const int rsub = lane >> 3, c = lane & 7;  // 8 lanes cover one 128-byte row
+    uint32_t g = 0;  // stages of the CTA so far
+    bool stop = false;
+    for (int t = blockIdx.x; t < total && !stop && !*abort_flag; t += gridDim.x) {
+      const Tile tl = decode_tile<MODE>(p, s, t);
+      const int nk = p.cls[tl.cls].k_dim / BK;
+      const bool routed = tl.cls == 0;
+      if (routed) {
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane + 32 * j, m = tl.mt * BM + r;
+          int tok = -1;
+          if (m < tl.rows) {
+            tok = p.token_of_row[tl.row0 + m];
+            if (tok < 0 || tok >= p.T) { raise_error(kErrIndex); tok = -1; }
+          }
+          rowsrc[r] = tok;
+        }
+        __syncwarp();
+      }
+      for (int kb = 0; kb < nk; ++kb, ++g) {
+        if (static_cast<int>(g & 3u) != slot) continue;
+        if (!mbar_wait(&s.empty[slot], ((g >> 2) & 1u) ^ 1u, abort_flag)) { stop = true; break; }
+        if (routed) {
+          const uint32_t sa = smem_u32(ring + slot * A_BYTES);
+          const __nv_bfloat16* xk = p.x_rows + kb * BK + c * 8;
+#pragma unroll 8
+          for (int j = 0; j < BM / 4; ++j) {
+            const int r = 4 * j + rsub;
+            const int tok = rowsrc[r];
+            if (tok >= 0) cp_async_16(sa + sw128_offset(r, c), xk + static_cast<size_t>(tok) * p.d, pol_x);
+          }
+          cp_async_wait_all();
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.full[slot]);
+      }
+    }
+    cp_async_wait_all();
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -378,18 +444,19 @@ void experts_scratch_carve(const moe_cfg_t& c, void* ws, void** h, float** h_sca
     *h_scales = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(hr + hs, 256));
 }
 
-template <int MODE>
+template <int MODE, bool GATHER>
 static cudaError_t launch_bf16_gemm(const bf16gemm::Params& prm, cudaStream_t st) {
   using namespace bf16gemm;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(experts_bf16_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(experts_bf16_kernel<MODE, GATHER>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  experts_bf16_kernel<MODE><<<sm_count(), THREADS, kSmemBytes, st>>>(prm);
+  experts_bf16_kernel<MODE, GATHER>
+      <<<sm_count(), GATHER ? THREADS_GATHER : THREADS, kSmemBytes, st>>>(prm);
   return cudaGetLastError();
 }
 
@@ -404,12 +471,18 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
 
-  // ---- gate/up: A = x_perm / x, B = W13
+  // ---- gate/up: A = x_perm (or, gathering, x[token_of_row]) / x, B = W13
+  const bool gather = a.token_of_row != nullptr;
   Params g{};
   g.offsets = a.offsets; g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
   g.inter = I; g.d = c.d;
-  CUresult r = encode_tensor_map_2d(&g.a_map[0], BF, const_cast<void*>(a.x_perm), c.d, tk,
-                                    static_cast<uint64_t>(c.d) * 2, BK, BM, SW);
+  g.token_of_row = a.token_of_row;
+  g.x_rows = static_cast<const __nv_bfloat16*>(a.x);
+  // (gathering never reads the routed A map; it is encoded over x to stay valid)
+  CUresult r = gather ? encode_tensor_map_2d(&g.a_map[0], BF, const_cast<void*>(a.x), c.d, c.T,
+                                             static_cast<uint64_t>(c.d) * 2, BK, BM, SW)
+                      : encode_tensor_map_2d(&g.a_map[0], BF, const_cast<void*>(a.x_perm), c.d, tk,
+                                             static_cast<uint64_t>(c.d) * 2, BK, BM, SW);
   if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[0], BF, a.w13, c.E, I, c.d, 2, BK);
   if (r == CUDA_SUCCESS && has_shared) {
     r = encode_tensor_map_2d(&g.a_map[1], BF, const_cast<void*>(a.x), c.d, c.T,
@@ -422,7 +495,7 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   g.cls[0] = ClassDesc{h_routed, I, I, c.d};
   g.cls[1] = ClassDesc{h_shared, Ns * I, Ns * I, c.d};
-  cudaError_t e = launch_bf16_gemm<GATEUP>(g, st);
+  cudaError_t e = gather ? launch_bf16_gemm<GATEUP, true>(g, st) : launch_bf16_gemm<GATEUP, false>(g, st);
   if (e != cudaSuccess) return e;
 
   // ---- down: A = h, B = W2
@@ -447,7 +520,7 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   dn.cls[0] = ClassDesc{static_cast<__nv_bfloat16*>(a.y_perm), c.d, c.d, I};
   dn.cls[1] = ClassDesc{static_cast<__nv_bfloat16*>(a.y_shared), c.d, c.d, Ns * I};
-  return launch_bf16_gemm<DOWN>(dn, st);
+  return launch_bf16_gemm<DOWN, false>(dn, st);
 }
 
 }  // namespace moe

@@ -73,6 +73,7 @@ struct ExpertsArgs {
   const float* ws2_scales;
   void* y_perm;
   void* y_shared;
+  const int32_t* token_of_row;  // non-null: gate/up gathers its routed A rows from x
   void* h;            // workspace: routed rows [T*K, I] then shared rows [T, Ns*I]
   float* h_scales;    // FP8: [T*K, I/128] then [T, Ns*I/128]
 };

@@ -177,6 +177,39 @@ moe_status_t moe_experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
   return from_cuda(e);
 }
 
+moe_status_t moe_experts_grouped_gather(const moe_cfg_t* cfg, const void* x,
+                                        const float* x_scales, const int32_t* token_of_row,
+                                        const int32_t* offsets, const void* w13,
+                                        const float* w13_scales, const void* w2,
+                                        const float* w2_scales, const void* ws13,
+                                        const float* ws13_scales, const void* ws2,
+                                        const float* ws2_scales, void* y_perm, void* y_shared,
+                                        void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (c.dtype != MOE_DTYPE_BF16) return MOE_ERR_SHAPE;
+  if (x == nullptr || token_of_row == nullptr || offsets == nullptr || w13 == nullptr ||
+      w2 == nullptr || y_perm == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0 && (ws13 == nullptr || ws2 == nullptr || y_shared == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, x_scales, token_of_row, offsets, w13, w13_scales, w2, w2_scales,
+                        ws13, ws13_scales, ws2, ws2_scales, y_perm, y_shared, ws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  if (ws_bytes < experts_scratch_bytes(c)) return MOE_ERR_WORKSPACE;
+  ExpertsArgs a{};
+  a.cfg = &c;
+  a.x = x;
+  a.token_of_row = token_of_row;
+  a.offsets = offsets;
+  a.w13 = w13; a.w2 = w2; a.ws13 = ws13; a.ws2 = ws2;
+  a.y_perm = y_perm; a.y_shared = c.n_shared > 0 ? y_shared : nullptr;
+  experts_scratch_carve(c, ws, &a.h, &a.h_scales);
+  return from_cuda(launch_experts_bf16(a, as_stream(stream)));
+}
+
 moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y_perm, const void* y_shared,
                          const int32_t* row_of_slot, const float* topk_w, void* out, void* stream) {
   moe_status_t st = moe_check_cfg(cfg);

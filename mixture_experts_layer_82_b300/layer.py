@@ -6,8 +6,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_combine,
-               moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes)
+from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_experts_grouped_gather,
+               moe_combine, moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes)
 
 
 def _quantize(w, stream=None):
@@ -27,8 +27,10 @@ class MoELayer:
     in bf16 (fp32 for the fp32 kind).  For the fp8 kind the expert weights
     are quantised once here (128 x 128 blocks)."""
 
-    def __init__(self, cfg: LayerCfg, router_w, bias, w13, w2, ws13=None, ws2=None):
+    def __init__(self, cfg: LayerCfg, router_w, bias, w13, w2, ws13=None, ws2=None,
+                 gather=False):
         self.cfg = cfg
+        self.gather = gather
         dev = router_w.device
         self.router_w, self.bias = router_w, bias
         T, d, E, K, I, ns = cfg.T, cfg.d, cfg.E, cfg.k, cfg.inter, cfg.n_shared
@@ -65,24 +67,34 @@ class MoELayer:
         self.ws = torch.empty(moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
 
     def forward(self, x, stream=None, update_bias=True, affinity_out=None, affinity_in=None,
-                expert_events=None):
+                expert_events=None, gather=None):
         """One forward step on ``x`` [T, d].  ``expert_events`` (a pair of
         torch.cuda.Event) are recorded on ``stream`` around the grouped
-        expert GEMMs, for timing them inside a step."""
+        expert GEMMs, for timing them inside a step.  ``gather`` (default:
+        ``self.gather``) folds the permute into the gate/up GEMM
+        (moe_experts_grouped_gather; bf16 kind)."""
         c = self.cfg
+        gather = self.gather if gather is None else gather
         moe_route(c, x, self.router_w, self.bias, self.topk_idx, self.topk_w, self.counts,
                   self.offsets, self.row_of_slot, self.token_of_row, self.ws,
                   affinity_in=affinity_in, affinity_out=affinity_out, stream=stream)
-        moe_permute(c, x, self.token_of_row, self.x_perm, self.x_perm_s, self.x_q, self.x_q_s,
-                    stream=stream)
-        shared_in = self.x_q if c.dtype == "fp8" else x
-        if expert_events is not None:
-            expert_events[0].record(stream)
-        moe_experts_grouped(c, self.x_perm, shared_in, self.offsets, self.w13, self.w2,
-                            self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
-                            x_perm_scales=self.x_perm_s, x_scales=self.x_q_s,
-                            w13_scales=self.w13_s, w2_scales=self.w2_s,
-                            ws13_scales=self.ws13_s, ws2_scales=self.ws2_s, stream=stream)
+        if gather:
+            if expert_events is not None:
+                expert_events[0].record(stream)
+            moe_experts_grouped_gather(c, x, self.token_of_row, self.offsets, self.w13, self.w2,
+                                       self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
+                                       stream=stream)
+        else:
+            moe_permute(c, x, self.token_of_row, self.x_perm, self.x_perm_s, self.x_q,
+                        self.x_q_s, stream=stream)
+            shared_in = self.x_q if c.dtype == "fp8" else x
+            if expert_events is not None:
+                expert_events[0].record(stream)
+            moe_experts_grouped(c, self.x_perm, shared_in, self.offsets, self.w13, self.w2,
+                                self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
+                                x_perm_scales=self.x_perm_s, x_scales=self.x_q_s,
+                                w13_scales=self.w13_s, w2_scales=self.w2_s,
+                                ws13_scales=self.ws13_s, ws2_scales=self.ws2_s, stream=stream)
         if expert_events is not None:
             expert_events[1].record(stream)
         moe_combine(c, self.y_perm, self.y_shared, self.row_of_slot, self.topk_w, self.out,
