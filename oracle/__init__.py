@@ -27,6 +27,7 @@ from .moe_oracle import (  # noqa: F401
     moe_layer_forward,
     moe_layer_tokens,
     load_spread,
+    sequence_balance,
 )
 from .fp8 import (  # noqa: F401
     E4M3_MAX,

@@ -259,6 +259,40 @@ def load_spread(counts):
     }
 
 
+def sequence_balance(affinity, topk_idx, seq_len, alpha=1e-4):
+    """Sequence-wise balance statistic L_Bal = alpha * sum_i f_i P_i per
+    sequence (auxiliary-loss-free paragraph: a complementary sequence-wise
+    balance loss with a small factor; training hyper-parameters paragraph:
+    alpha = 0.0001).  The pages do not define f_i and P_i; the reading here:
+    for a sequence of L consecutive tokens,
+        f_i = E / (K L) * #{(t, k) in the sequence: expert i chosen}
+        P_i = (1 / L) * sum_t s_{i,t} / sum_j s_{j,t}
+    so an even split of the selections gives f_i = 1.
+
+    ``affinity`` [T, E] (the unbiased s), ``topk_idx`` [T, K]; T must be a
+    multiple of ``seq_len``.  Returns (f [n_seq, E], P [n_seq, E],
+    loss [n_seq]) in fp64."""
+    s = np.asarray(affinity, dtype=np.float64)
+    idx = np.asarray(topk_idx)
+    T, E = s.shape
+    K = idx.shape[1]
+    assert T % seq_len == 0
+    n = T // seq_len
+    f = np.zeros((n, E))
+    P = np.zeros((n, E))
+    loss = np.zeros(n)
+    for q in range(n):
+        rows = range(q * seq_len, (q + 1) * seq_len)
+        for t in rows:
+            for e in idx[t]:
+                f[q, int(e)] += 1.0
+            P[q] += s[t] / s[t].sum()
+        f[q] *= E / (K * seq_len)
+        P[q] /= seq_len
+        loss[q] = alpha * float(np.dot(f[q], P[q]))
+    return f, P, loss
+
+
 # --------------------------------------------------------------------------
 # Whole layer
 # --------------------------------------------------------------------------

@@ -455,3 +455,50 @@ def test_sampled_tokens_match_whole_layer():
     y = oracle.moe_layer_tokens(ins[0][rows], r["topk_idx"][rows], r["topk_w"][rows],
                                 ins[3], ins[4], ins[5], ins[6])
     np.testing.assert_allclose(y, r["out"][rows], rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------- sequence-wise balance statistic
+
+def test_sequence_balance_invariants():
+    """sum_i f_i = E for every sequence; equal affinities give P_i = 1/E and
+    so L = alpha whatever the routing; alpha scales the loss linearly."""
+    rng = np.random.default_rng(11)
+    T, E, K, L = 96, 16, 3, 24
+    s = rng.random((T, E)) + 0.05
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)])
+    f, P, loss = oracle.sequence_balance(s, idx, L, alpha=1e-4)
+    np.testing.assert_allclose(f.sum(axis=1), E, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    f2, P2, loss2 = oracle.sequence_balance(np.full((T, E), 0.37), idx, L, alpha=1e-4)
+    np.testing.assert_allclose(P2, 1.0 / E, rtol=1e-14)
+    np.testing.assert_allclose(loss2, 1e-4, rtol=1e-12)
+    _, _, loss3 = oracle.sequence_balance(s, idx, L, alpha=3e-3)
+    np.testing.assert_allclose(loss3, loss * 30, rtol=1e-12)
+
+
+def test_sequence_balance_hand_example():
+    """Two tokens, E = 4, K = 1, one sequence.  Token 0 chooses expert 2 with
+    s = [1, 1, 2, 0]; token 1 chooses expert 2 with s = [0, 0, 1, 1].
+    f = 4 / (1 * 2) * [0, 0, 2, 0] = [0, 0, 4, 0];
+    P = ([.25, .25, .5, 0] + [0, 0, .5, .5]) / 2 = [.125, .125, .5, .25];
+    L = alpha * 4 * 0.5 = 2 alpha."""
+    s = np.array([[1.0, 1.0, 2.0, 0.0], [0.0, 0.0, 1.0, 1.0]])
+    idx = np.array([[2], [2]])
+    f, P, loss = oracle.sequence_balance(s, idx, 2, alpha=1e-4)
+    np.testing.assert_array_equal(f[0], [0, 0, 4, 0])
+    np.testing.assert_allclose(P[0], [0.125, 0.125, 0.5, 0.25], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(loss, [2e-4], rtol=1e-13)
+
+
+def test_sequence_balance_splits_sequences():
+    """Sequences are independent: the statistic of a batch of two sequences
+    is the statistic of each sequence alone."""
+    rng = np.random.default_rng(12)
+    T, E, K = 40, 8, 2
+    s = rng.random((T, E))
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)])
+    f, P, loss = oracle.sequence_balance(s, idx, 20)
+    fa, Pa, la = oracle.sequence_balance(s[:20], idx[:20], 20)
+    fb, Pb, lb = oracle.sequence_balance(s[20:], idx[20:], 20)
+    np.testing.assert_array_equal(f, np.concatenate([fa, fb]))
+    np.testing.assert_array_equal(loss, np.concatenate([la, lb]))
