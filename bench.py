@@ -241,17 +241,35 @@ def load_balance(moe, shape, L, steps):
     ws = torch.empty(moe.moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
     aff = torch.empty(T, E, dtype=torch.float32, device=dev)
     bias = L["bias"].clone()
+    # sequence-wise balance statistic of the batch taken as one sequence
+    f = torch.empty(1, E, dtype=torch.float32, device=dev)
+    p = torch.empty_like(f)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
     moe.moe_route(cfg, L["x"], L["router_w"], bias, *bufs, ws, affinity_out=aff)
+    moe.moe_balance_stat(cfg, aff, bufs[0], T, f, p, loss, ws)
     before = load_stats(bufs[2].cpu().numpy(), T, K)
+    before["seq_balance_stat"] = float(loss.item())
     for i in range(steps):
         if i:
             moe.moe_route(cfg, None, None, bias, *bufs, ws, affinity_in=aff)
         moe.moe_bias_update(cfg, bufs[2], bias)
     moe.moe_route(cfg, None, None, bias, *bufs, ws, affinity_in=aff)
     after = load_stats(bufs[2].cpu().numpy(), T, K)
+    # time the statistic's two kernels (after warm-up)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        moe.moe_balance_stat(cfg, aff, bufs[0], T, f, p, loss, ws)
+    e0.record()
+    for _ in range(10):
+        moe.moe_balance_stat(cfg, aff, bufs[0], T, f, p, loss, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    after["seq_balance_stat"] = float(loss.item())
     if moe.moe_get_device_error() != 0:
         raise RuntimeError("device error in the load-balance steps")
-    return {"bias_steps": steps, "gamma": shape.gamma, "before": before, "after": after}
+    return {"bias_steps": steps, "gamma": shape.gamma, "before": before, "after": after,
+            "seq_balance": {"alpha": 1e-4, "seq_len": T,
+                            "us_per_call": 1e3 * e0.elapsed_time(e1) / 10}}
 
 
 # ----------------------------------------------------------- CPU baseline

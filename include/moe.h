@@ -242,6 +242,32 @@ moe_status_t moe_bias_update(const moe_cfg_t* cfg, const int32_t* counts,
                              float* bias, void* stream);
 
 /*
+ * moe_balance_stat - the sequence-wise balance statistic
+ *     L_Bal = alpha * sum_i f_i P_i
+ * of every sequence of seq_len consecutive tokens (auxiliary-loss-free
+ * paragraph: the complementary sequence-wise balance loss, with a small
+ * factor alpha, 0.0001 in the training hyper-parameters).  The pages do not
+ * define f_i and P_i; here
+ *     f_i = E / (K * seq_len) * (selections of expert i in the sequence)
+ *     P_i = mean over the sequence's tokens of s_i / sum_j s_j
+ * so an even split gives f_i = 1.  Forward statistic only (no gradient).
+ *
+ *   affinity  [T, E]  fp32 unbiased s (moe_route's affinity_out)
+ *   topk_idx  [T, K]  int32 from moe_route
+ *   seq_len   divides T; T / seq_len <= 65535 sequences
+ *   f_out, p_out [T / seq_len, E] fp32 out; loss_out [T / seq_len] fp32 out
+ *   ws, ws_bytes  scratch for per-chunk partial sums: 2 * align256(4 *
+ *                 (T / seq_len) * ceil(seq_len / 256) * E) bytes, which
+ *                 moe_workspace_bytes(cfg) covers for seq_len >= 2
+ *                 (MOE_ERR_WORKSPACE if too small)
+ * Sums are fp32 in a fixed order (deterministic).
+ */
+moe_status_t moe_balance_stat(const moe_cfg_t* cfg, const float* affinity,
+                              const int32_t* topk_idx, int32_t seq_len, float alpha,
+                              float* f_out, float* p_out, float* loss_out, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/*
  * moe_quantize_weights_fp8 - offline utility: quantise `n_mats` bf16
  * matrices [rows, cols] (contiguous, cols % 128 == 0) to E4M3 in 128 x 128
  * blocks (fine-grained quantisation paragraph): scale = fl32(amax / 448)

@@ -39,7 +39,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR
 EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_bytes",
             "moe_route", "moe_permute", "moe_experts_grouped", "moe_combine",
             "moe_bias_update", "moe_quantize_weights_fp8", "moe_get_device_error",
-            "moe_route_static_scratch", "moe_experts_grouped_gather")
+            "moe_route_static_scratch", "moe_experts_grouped_gather", "moe_balance_stat")
 
 
 class MoeCfg(ctypes.Structure):
@@ -76,6 +76,9 @@ _lib.moe_experts_grouped.restype = ctypes.c_int
 _lib.moe_experts_grouped.argtypes = [_CFG] + [_P] * 15 + [_P, ctypes.c_size_t, _P]
 _lib.moe_experts_grouped_gather.restype = ctypes.c_int
 _lib.moe_experts_grouped_gather.argtypes = [_CFG] + [_P] * 14 + [_P, ctypes.c_size_t, _P]
+_lib.moe_balance_stat.restype = ctypes.c_int
+_lib.moe_balance_stat.argtypes = [_CFG, _P, _P, ctypes.c_int32, ctypes.c_float, _P, _P, _P, _P,
+                                  ctypes.c_size_t, _P]
 _lib.moe_combine.restype = ctypes.c_int
 _lib.moe_combine.argtypes = [_CFG] + [_P] * 5 + [_P]
 _lib.moe_bias_update.restype = ctypes.c_int
@@ -248,6 +251,17 @@ def moe_experts_grouped_gather(cfg, x, token_of_row, offsets, w13, w2, ws13, ws2
         _ptr(ws2_scales, "ws2_scales", torch.float32, allow_none=True),
         _ptr(y_perm, "y_perm", _X), _ptr(y_shared, "y_shared", _X, allow_none=True),
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_balance_stat(cfg, affinity, topk_idx, seq_len, f_out, p_out, loss_out, ws, alpha=1e-4,
+                     stream=None):
+    """Sequence-wise balance statistic alpha * sum_i f_i P_i per sequence."""
+    _check("moe_balance_stat", _lib.moe_balance_stat(
+        _cfg(cfg), _ptr(affinity, "affinity", torch.float32),
+        _ptr(topk_idx, "topk_idx", torch.int32), int(seq_len), float(alpha),
+        _ptr(f_out, "f_out", torch.float32), _ptr(p_out, "p_out", torch.float32),
+        _ptr(loss_out, "loss_out", torch.float32), _ptr(ws, "ws"),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_combine(cfg, y_perm, y_shared, row_of_slot, topk_w, out, stream=None):

@@ -40,6 +40,10 @@ cudaError_t launch_route_assign(const moe_cfg_t& c, const int32_t* topk_idx,
                                 int32_t* token_of_row, cudaStream_t s);
 cudaError_t launch_bias_update(const moe_cfg_t& c, const int32_t* counts, float* bias,
                                cudaStream_t s);
+size_t balance_scratch_bytes(const moe_cfg_t& c, int seq_len);
+cudaError_t launch_balance_stat(const moe_cfg_t& c, const float* affinity, const int32_t* topk_idx,
+                                int seq_len, float alpha, float* f_out, float* p_out, float* loss,
+                                void* ws, cudaStream_t s);
 
 // permute / combine / quantise
 cudaError_t launch_permute(const moe_cfg_t& c, const void* x, const int32_t* token_of_row,

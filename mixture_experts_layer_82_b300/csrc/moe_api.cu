@@ -233,6 +233,26 @@ moe_status_t moe_bias_update(const moe_cfg_t* cfg, const int32_t* counts, float*
   return from_cuda(launch_bias_update(*cfg, counts, bias, as_stream(stream)));
 }
 
+moe_status_t moe_balance_stat(const moe_cfg_t* cfg, const float* affinity,
+                              const int32_t* topk_idx, int32_t seq_len, float alpha, float* f_out,
+                              float* p_out, float* loss_out, void* ws, size_t ws_bytes,
+                              void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (affinity == nullptr || topk_idx == nullptr || f_out == nullptr || p_out == nullptr ||
+      loss_out == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (seq_len < 1 || c.T % seq_len != 0 || !(alpha == alpha)) return MOE_ERR_INVALID_ARG;
+  if (c.T / seq_len > 65535) return MOE_ERR_SHAPE;
+  const void* ptrs[] = {affinity, topk_idx, f_out, p_out, loss_out, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  if (ws_bytes < balance_scratch_bytes(c, seq_len)) return MOE_ERR_WORKSPACE;
+  return from_cuda(launch_balance_stat(c, affinity, topk_idx, seq_len, alpha, f_out, p_out,
+                                       loss_out, ws, as_stream(stream)));
+}
+
 moe_status_t moe_quantize_weights_fp8(const void* w_bf16, int32_t n_mats, int32_t rows,
                                       int32_t cols, void* q, float* scales, void* stream) {
   if (w_bf16 == nullptr || q == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;

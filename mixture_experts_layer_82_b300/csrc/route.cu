@@ -392,4 +392,107 @@ cudaError_t launch_bias_update(const moe_cfg_t& c, const int32_t* counts, float*
   return cudaGetLastError();
 }
 
+// ------------------------------------------------ sequence-wise balance stat
+// L_Bal = alpha * sum_i f_i P_i per sequence of L consecutive tokens
+// ("DeepSeek-V3 Technical Report", auxiliary-loss-free paragraph: the
+// complementary sequence-wise balance loss; alpha from the training
+// hyper-parameters).  f_i = E / (K L) * selections of expert i in the
+// sequence, P_i = mean over the sequence of s_i / sum_j s_j.
+constexpr int kBalWarps = 8;
+constexpr int kBalChunk = 256;  // tokens of a sequence per CTA
+
+// Partial sums of one (sequence, 32-expert chunk, 256-token chunk): warp w
+// takes tokens w, w + 8, ... of the token chunk; lane j owns expert
+// 32 * blockIdx.y + j.  Writes sum_t s_e / sum_j s_j and the selection
+// count of every owned expert to part_p / part_c [n_seq][chunks][E].
+__global__ void __launch_bounds__(kBalWarps * 32) balance_partial_kernel(
+    const float* __restrict__ s, const int32_t* __restrict__ topk_idx, int E, int K, int L,
+    float* __restrict__ part_p, int* __restrict__ part_c) {
+  __shared__ float ps[kBalWarps][32];
+  __shared__ int cs[kBalWarps][32];
+  const int q = blockIdx.x, e0 = blockIdx.y * 32, ch = blockIdx.z, nch = gridDim.z;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int e = e0 + lane;
+  const int i0 = ch * kBalChunk, i1 = min(L, i0 + kBalChunk);
+  float p = 0.f;
+  int cnt = 0;
+  for (int i = i0 + warp; i < i1; i += kBalWarps) {
+    const size_t t = static_cast<size_t>(q) * L + i;
+    const float* row = s + t * E;
+    float rs = 0.f;
+    for (int j = lane; j < E; j += 32) rs += row[j];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, off);
+    const int my_idx = lane < K ? topk_idx[t * K + lane] : -1;
+    for (int k = 0; k < K; ++k) cnt += __shfl_sync(0xffffffffu, my_idx, k) == e ? 1 : 0;
+    if (e < E) p += __fdiv_rn(row[e], rs);
+  }
+  ps[warp][lane] = p;
+  cs[warp][lane] = cnt;
+  __syncthreads();
+  if (warp == 0 && e < E) {
+    float pt = 0.f;
+    int ct = 0;
+    for (int w = 0; w < kBalWarps; ++w) { pt += ps[w][lane]; ct += cs[w][lane]; }
+    const size_t o = (static_cast<size_t>(q) * nch + ch) * E + e;
+    part_p[o] = pt;
+    part_c[o] = ct;
+  }
+}
+
+// One CTA per sequence: f and P of every expert from the partials (summed
+// in chunk order), then loss = alpha * sum_i f_i P_i (each thread sums its
+// experts in order, then a fixed reduction tree).
+__global__ void __launch_bounds__(256) balance_final_kernel(
+    const float* __restrict__ part_p, const int* __restrict__ part_c, int E, int K, int L, int nch,
+    float alpha, float* __restrict__ f_out, float* __restrict__ p_out, float* __restrict__ loss) {
+  __shared__ float red[256];
+  const int q = blockIdx.x;
+  float acc = 0.f;
+  for (int e = threadIdx.x; e < E; e += 256) {
+    float pt = 0.f;
+    int ct = 0;
+    for (int ch = 0; ch < nch; ++ch) {
+      const size_t o = (static_cast<size_t>(q) * nch + ch) * E + e;
+      pt += part_p[o];
+      ct += part_c[o];
+    }
+    const float P = __fdiv_rn(pt, static_cast<float>(L));
+    const float f = static_cast<float>(static_cast<double>(E) * ct / (static_cast<double>(K) * L));
+    p_out[static_cast<size_t>(q) * E + e] = P;
+    f_out[static_cast<size_t>(q) * E + e] = f;
+    acc = fmaf(f, P, acc);
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) loss[q] = alpha * red[0];
+}
+
+size_t balance_scratch_bytes(const moe_cfg_t& c, int seq_len) {
+  const size_t n = static_cast<size_t>(c.T / seq_len) * ceil_div(seq_len, kBalChunk) * c.E;
+  return align_up(n * 4, 256) * 2;
+}
+
+cudaError_t launch_balance_stat(const moe_cfg_t& c, const float* affinity, const int32_t* topk_idx,
+                                int seq_len, float alpha, float* f_out, float* p_out, float* loss,
+                                void* ws, cudaStream_t st) {
+  const int n_seq = c.T / seq_len;
+  const int nch = ceil_div(seq_len, kBalChunk);
+  const size_t n = static_cast<size_t>(n_seq) * nch * c.E;
+  float* part_p = static_cast<float*>(ws);
+  int* part_c = reinterpret_cast<int*>(static_cast<char*>(ws) + align_up(n * 4, 256));
+  dim3 grid(n_seq, ceil_div(c.E, 32), nch);
+  balance_partial_kernel<<<grid, kBalWarps * 32, 0, st>>>(affinity, topk_idx, c.E, c.K, seq_len,
+                                                          part_p, part_c);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  balance_final_kernel<<<n_seq, 256, 0, st>>>(part_p, part_c, c.E, c.K, seq_len, nch, alpha, f_out,
+                                              p_out, loss);
+  return cudaGetLastError();
+}
+
 }  // namespace moe
