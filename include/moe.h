@@ -313,6 +313,16 @@ moe_status_t moe_route_static_scratch(const moe_cfg_t* cfg, const void* x,
                                       int32_t* offsets, int32_t* row_of_slot,
                                       int32_t* token_of_row, void* stream);
 
+/*
+ * moe_selftest_wait - failure-detection self test.  One thread waits, with
+ * the same bounded mbarrier wait the GEMM kernels use, on a barrier that
+ * nothing arrives on; after limit_ns nanoseconds (1 .. 10^10) it gives up
+ * and sets the timeout bit of the error word, so that the next
+ * moe_get_device_error() returns MOE_ERR_TIMEOUT.  Nothing traps and the
+ * device stays usable.  MOE_ERR_INVALID_ARG for a limit outside the range.
+ */
+moe_status_t moe_selftest_wait(int64_t limit_ns, void* stream);
+
 /* Synchronises `stream`, returns the device error word (MOE_OK if clear,
  * MOE_ERR_TIMEOUT if a wait gave up, MOE_ERR_DEVICE for any other device
  * check) and clears it. */

@@ -39,7 +39,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR
 EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_bytes",
             "moe_route", "moe_permute", "moe_experts_grouped", "moe_combine",
             "moe_bias_update", "moe_quantize_weights_fp8", "moe_get_device_error",
-            "moe_route_static_scratch", "moe_experts_grouped_gather", "moe_balance_stat")
+            "moe_route_static_scratch", "moe_experts_grouped_gather", "moe_balance_stat",
+            "moe_selftest_wait")
 
 
 class MoeCfg(ctypes.Structure):
@@ -86,6 +87,8 @@ _lib.moe_bias_update.argtypes = [_CFG, _P, _P, _P]
 _lib.moe_quantize_weights_fp8.restype = ctypes.c_int
 _lib.moe_quantize_weights_fp8.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                           _P, _P, _P]
+_lib.moe_selftest_wait.restype = ctypes.c_int
+_lib.moe_selftest_wait.argtypes = [ctypes.c_int64, _P]
 _lib.moe_get_device_error.restype = ctypes.c_int
 _lib.moe_get_device_error.argtypes = [_P]
 _lib.moe_route_static_scratch.restype = ctypes.c_int
@@ -283,6 +286,12 @@ def moe_quantize_weights_fp8(w, q, scales, stream=None):
     _check("moe_quantize_weights_fp8", _lib.moe_quantize_weights_fp8(
         _ptr(w, "w", torch.bfloat16), w3.shape[0], w3.shape[1], w3.shape[2],
         _ptr(q, "q", _F8), _ptr(scales, "scales", torch.float32), _stream(stream)))
+
+
+def moe_selftest_wait(limit_ns, stream=None):
+    """Failure-detection self test: a bounded device wait that must give up
+    after limit_ns and set the timeout bit of the error word."""
+    _check("moe_selftest_wait", _lib.moe_selftest_wait(int(limit_ns), _stream(stream)))
 
 
 def moe_get_device_error(stream=None):

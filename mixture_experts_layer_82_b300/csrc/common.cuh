@@ -81,7 +81,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // after kWaitLimitNs, or as soon as *abort is set by another thread of the
 // block; on giving up it sets *abort and the error word and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -89,7 +90,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort) return false;
-    if ((++spins & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+    if ((++spins & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       raise_error(kErrTimeout);
       return false;

@@ -13,6 +13,21 @@ namespace {
 
 constexpr int32_t kVersion = 100;  // 0.1.0
 
+// Failure-detection self test: thread 0 waits, with the bounded wait of the
+// GEMM kernels, on a barrier that nothing arrives on, so the wait gives up
+// after limit_ns and sets the timeout bit of the error word.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, limit_ns);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -261,6 +276,12 @@ moe_status_t moe_quantize_weights_fp8(const void* w_bf16, int32_t n_mats, int32_
   if (!aligned16(w_bf16) || !aligned16(q) || !aligned16(scales)) return MOE_ERR_ALIGN;
   return from_cuda(launch_quantize_weights_fp8(w_bf16, n_mats, rows, cols, q, scales,
                                                as_stream(stream)));
+}
+
+moe_status_t moe_selftest_wait(int64_t limit_ns, void* stream) {
+  if (limit_ns < 1 || limit_ns > 10000000000LL) return MOE_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(static_cast<uint64_t>(limit_ns));
+  return from_cuda(cudaGetLastError());
 }
 
 moe_status_t moe_get_device_error(void* stream) {
