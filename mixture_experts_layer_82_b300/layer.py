@@ -67,13 +67,15 @@ class MoELayer:
         self.ws = torch.empty(moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
 
     def forward(self, x, stream=None, update_bias=True, affinity_out=None, affinity_in=None,
-                expert_events=None, gather=None):
-        """One forward step on ``x`` [T, d].  ``expert_events`` (a pair of
-        torch.cuda.Event) are recorded on ``stream`` around the grouped
-        expert GEMMs, for timing them inside a step.  ``gather`` (default:
-        ``self.gather``) folds the permute into the gate/up GEMM
-        (moe_experts_grouped_gather; bf16 kind)."""
+                expert_events=None, gather=None, out=None):
+        """One forward step on ``x`` [T, d]; returns the layer output, written
+        to ``out`` when given (else to the layer's own buffer).
+        ``expert_events`` (a pair of torch.cuda.Event) are recorded on
+        ``stream`` around the grouped expert GEMMs, for timing them inside a
+        step.  ``gather`` (default: ``self.gather``) folds the permute into
+        the gate/up GEMM (moe_experts_grouped_gather; bf16 kind)."""
         c = self.cfg
+        out = self.out if out is None else out
         gather = self.gather if gather is None else gather
         moe_route(c, x, self.router_w, self.bias, self.topk_idx, self.topk_w, self.counts,
                   self.offsets, self.row_of_slot, self.token_of_row, self.ws,
@@ -97,8 +99,8 @@ class MoELayer:
                                 ws13_scales=self.ws13_s, ws2_scales=self.ws2_s, stream=stream)
         if expert_events is not None:
             expert_events[1].record(stream)
-        moe_combine(c, self.y_perm, self.y_shared, self.row_of_slot, self.topk_w, self.out,
+        moe_combine(c, self.y_perm, self.y_shared, self.row_of_slot, self.topk_w, out,
                     stream=stream)
         if update_bias:
             moe_bias_update(c, self.counts, self.bias, stream=stream)
-        return self.out
+        return out

@@ -282,3 +282,16 @@ def test_quantize_weights_fp8_bitwise():
         oq, os_ = oracle.quantize_weight_128x128(host(w[m]))
         assert np.array_equal(host(s[m]).view(np.uint32), os_.view(np.uint32))
         assert np.array_equal(q[m].float().cpu().numpy().astype(np.float64), oq)
+
+
+def test_forward_into_a_given_output_buffer():
+    """forward(x, out=buf) writes the same bits into buf as into the layer's
+    own output buffer (the end-to-end benchmark double-buffers outputs)."""
+    shape = shape_with(CONFIGS["mid_bf16"], T=300)
+    L, cfg, layer = _layer(shape)
+    a = layer.forward(L["x"], update_bias=False).clone()
+    buf = torch.full_like(a, 3.0)
+    b = layer.forward(L["x"], update_bias=False, out=buf)
+    assert b.data_ptr() == buf.data_ptr()
+    assert torch.equal(buf.view(torch.int16), a.view(torch.int16))
+    assert moe.moe_get_device_error() == 0
