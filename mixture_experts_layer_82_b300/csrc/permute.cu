@@ -17,12 +17,15 @@ namespace moe {
 
 constexpr int kRowWarps = 8;
 
+// Row copy by one warp.  The destination rows are written once and read
+// by a later kernel, so they are stored with the streaming hint (.cs): they
+// should not push the source rows (each read K times) out of L2.
 __device__ __forceinline__ void copy_row_bytes(char* __restrict__ dst, const char* __restrict__ src,
                                                size_t bytes, int lane) {
   const size_t nv = bytes / 16;
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
   uint4* d4 = reinterpret_cast<uint4*>(dst);
-  for (size_t i = lane; i < nv; i += 32) d4[i] = __ldg(s4 + i);
+  for (size_t i = lane; i < nv; i += 32) __stcs(d4 + i, __ldg(s4 + i));
   for (size_t i = nv * 16 + lane * 4; i < bytes; i += 128)
     *reinterpret_cast<uint32_t*>(dst + i) = *reinterpret_cast<const uint32_t*>(src + i);
 }
