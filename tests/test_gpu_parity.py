@@ -295,3 +295,29 @@ def test_forward_into_a_given_output_buffer():
     assert b.data_ptr() == buf.data_ptr()
     assert torch.equal(buf.view(torch.int16), a.view(torch.int16))
     assert moe.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    # the ABI's maximum of routed experts: 1024 experts in 32 groups, most
+    # segments empty or a few rows long
+    shape_with(CONFIGS["mid_bf16"], T=300, d=256, E=1024, n_groups=32, topk_groups=8, k=8,
+               n_shared=1, inter=128),
+    # d % 256 == 128 (the last down tile is half outside d), two shared experts
+    shape_with(CONFIGS["mid_bf16"], T=301, d=640, E=8, n_groups=4, topk_groups=2, k=2,
+               n_shared=2, inter=384),
+    # the smallest bf16 sizes: d = I = 128, no shared expert
+    shape_with(CONFIGS["mid_bf16"], T=130, d=128, E=16, n_groups=4, topk_groups=2, k=4,
+               n_shared=0, inter=128),
+], ids=lambda s: f"E{s.E}-d{s.d}-I{s.inter}-Ns{s.n_shared}")
+def test_layer_edge_shapes(shape):
+    L, cfg, layer = _layer(shape)
+    aff = torch.empty(shape.T, shape.E, dtype=torch.float32, device=DEV)
+    out = layer.forward(L["x"], affinity_out=aff, update_bias=False)
+    assert moe.moe_get_device_error() == 0
+    r = _oracle_layer(shape, L, host(aff))
+    assert np.array_equal(host(layer.topk_idx), r["topk_idx"])
+    assert np.array_equal(host(layer.offsets), r["offsets"])
+    assert rel_frobenius(host(layer.y_perm), r["y_perm"]) < TOL["bf16"]
+    if shape.n_shared:
+        assert rel_frobenius(host(layer.y_shared), r["y_shared"]) < TOL["bf16"]
+    assert rel_frobenius(host(out), r["out"]) < TOL["bf16"]
