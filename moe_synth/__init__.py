@@ -165,3 +165,11 @@ def make_tokens(shape: LayerShape, n_tokens, device="cpu", seed_offset=0):
     """Extra token batches of the same distribution (e.g. for calibration)."""
     g = _gen(torch.device(device), shape.seed + 7919 + seed_offset)
     return torch.randn(n_tokens, shape.d, generator=g, device=device, dtype=torch.float32)
+
+
+def make_grad(shape: LayerShape, device="cpu"):
+    """Gradient of a loss with respect to the layer output, dL/dy [T, d]:
+    standard normal values in the storage type (seeded per shape)."""
+    g = _gen(torch.device(device), shape.seed + 5003)
+    dy = torch.randn(shape.T, shape.d, generator=g, device=device, dtype=torch.float32)
+    return dy.to(storage_dtype(shape)).contiguous()

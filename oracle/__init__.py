@@ -45,3 +45,8 @@ from .moe_fp8 import (  # noqa: F401
     moe_layer_forward_fp8,
     moe_layer_tokens_fp8,
 )
+from .moe_backward import (  # noqa: F401
+    swiglu_ffn_backward,
+    gate_backward,
+    moe_layer_backward,
+)
