@@ -1,6 +1,6 @@
 /*
- * moe.h - C ABI of libmoe: the forward pass of one DeepSeekMoE layer on one
- * NVIDIA B300 (sm_103a).
+ * moe.h - C ABI of libmoe: the forward pass (and, for the BF16 kind, the
+ * backward pass) of one DeepSeekMoE layer on one NVIDIA B300 (sm_103a).
  *
  * The layer is the one of the "DeepSeek-V3 Technical Report":
  *   - DeepSeekMoE paragraph: token t's FFN output is the sum of N_s shared
@@ -18,6 +18,8 @@
  * One call per step of the layer:
  *     moe_route -> moe_permute -> moe_experts_grouped -> moe_combine
  *               -> moe_bias_update
+ * and, for training (BF16 kind), four calls for its backward pass (see
+ * "backward pass" below).
  *
  * Conventions shared by every call
  *   - All tensors are dense, row-major, in device memory allocated and owned
@@ -266,6 +268,113 @@ moe_status_t moe_balance_stat(const moe_cfg_t* cfg, const float* affinity,
                               const int32_t* topk_idx, int32_t seq_len, float alpha,
                               float* f_out, float* p_out, float* loss_out, void* ws,
                               size_t ws_bytes, void* stream);
+
+/*
+ * ------------------------------------------------------------ backward pass
+ * BF16 kind only (MOE_ERR_SHAPE otherwise; also for n_shared > 64).
+ *
+ * The chain rule of the layer above with the top-K selection held fixed (a
+ * choice has no gradient) and no gradient for the selection bias (it only
+ * steers the choice, auxiliary-loss-free paragraph).  Mixed precision
+ * framework paragraph: each linear has a Dgrad and a Wgrad GEMM next to
+ * its Fprop; DualPipe paragraph: the MLP backward splits into backward for
+ * input and backward for weights.  One step, given dL/dy (`dout`) and the
+ * forward's routing outputs:
+ *     moe_combine_backward -> moe_experts_backward_input
+ *         -> moe_route_backward        (dx and dL/de: input side complete)
+ *         -> moe_experts_backward_weights
+ * The weights call may run any time after the input call, on the same
+ * workspace (it reads the intermediates the input call left there).
+ *
+ * With a = x W1^T, b = x W3^T, h = silu(a) b, g = rho s / S:
+ *   dy_perm[row(t,k)] = g_{t,k} dout_t          dgate_{t,k} = dout_t . y_perm[row(t,k)]
+ *   dh = dy W2,  da = dh b silu'(a),  db = dh silu(a),  dx_e = [da | db] W13
+ *   dW2 = dy^T h,  dW13 = [da | db]^T x  (per expert, over its segment)
+ *   ds_k = rho / S (dgate_k - sum_j dgate_j s_j / S),  dlogit_k = ds_k s_k (1 - s_k)
+ *   dx_t = dx_shared_t + sum_k (dx_perm[row(t,k)] + dlogit_{t,k} e_{idx(t,k)})
+ *   drouter_w_i = sum over the tokens t that chose i of dlogit_{t,k} x_t
+ * All GEMMs accumulate in fp32; every stored intermediate and gradient is
+ * bf16 except dgate, dlogit and drouter_w (fp32).  Sums run in a fixed
+ * order: results are deterministic.
+ */
+
+/* Scratch of the backward calls: align256((T*K + T*N_s) * 3I * 2) bytes of
+ * expert intermediates ([a | b] then [da | db], and h; they must survive
+ * from moe_experts_backward_input to moe_experts_backward_weights) plus
+ * align256(T*K*4) bytes for moe_route_backward.  0 for a configuration the
+ * backward does not support. */
+size_t moe_backward_workspace_bytes(const moe_cfg_t* cfg);
+
+/*
+ * moe_combine_backward - gradient of moe_combine.
+ *   dout        [T, d]    bf16 dL/dy of the layer output
+ *   y_perm      [T*K, d]  bf16 routed expert outputs of the forward
+ *   row_of_slot [T, K], topk_w [T, K]  from moe_route
+ *   dy_perm     [T*K, d]  bf16 out: g_{t,k} dout_t at row(t,k)
+ *   dgate       [T, K]    fp32 out: dout_t . y_perm[row(t,k)]
+ * A row index outside [0, T*K) sets the error word; that slot is skipped.
+ */
+moe_status_t moe_combine_backward(const moe_cfg_t* cfg, const void* dout, const void* y_perm,
+                                  const int32_t* row_of_slot, const float* topk_w,
+                                  void* dy_perm, float* dgate, void* stream);
+
+/*
+ * moe_experts_backward_input - Dgrad of every expert FFN: recomputes
+ * [a | b] with the forward's grouped GEMM, then dh, the SwiGLU backward and
+ * dx, leaving [da | db] and h in `ws` for moe_experts_backward_weights.
+ *   x_perm [T*K, d], x [T, d]       bf16 forward inputs (routed / shared)
+ *   offsets [E + 1]                 from moe_route
+ *   w13, w2, ws13, ws2              as in moe_experts_grouped
+ *   dy_perm [T*K, d]                from moe_combine_backward
+ *   dout    [T, d]                  dL/dy (the shared experts' dy)
+ *   dx_perm [T*K, d]   bf16 out: routed experts' input gradient per row
+ *   dx_shared [T, d]   bf16 out: sum of the shared experts' input
+ *                      gradients (NULL if N_s = 0)
+ *   ws, ws_bytes       at least moe_backward_workspace_bytes(cfg)
+ */
+moe_status_t moe_experts_backward_input(const moe_cfg_t* cfg, const void* x_perm,
+                                        const void* x, const int32_t* offsets, const void* w13,
+                                        const void* w2, const void* ws13, const void* ws2,
+                                        const void* dy_perm, const void* dout, void* dx_perm,
+                                        void* dx_shared, void* ws, size_t ws_bytes,
+                                        void* stream);
+
+/*
+ * moe_experts_backward_weights - Wgrad of every expert FFN from the
+ * intermediates moe_experts_backward_input left in `ws` (same cfg, same
+ * offsets, workspace untouched in between except by moe_route_backward).
+ *   x_perm, x, offsets, dy_perm, dout   as for the input call
+ *   dw13 [E, 2I, d], dw2 [E, d, I]      bf16 out (an expert with no rows
+ *                                       gets zeros)
+ *   dws13 [N_s, 2I, d], dws2 [N_s, d, I] bf16 out (NULL if N_s = 0)
+ */
+moe_status_t moe_experts_backward_weights(const moe_cfg_t* cfg, const void* x_perm,
+                                          const void* x, const int32_t* offsets,
+                                          const void* dy_perm, const void* dout, void* dw13,
+                                          void* dw2, void* dws13, void* dws2, void* ws,
+                                          size_t ws_bytes, void* stream);
+
+/*
+ * moe_route_backward - gradient through the gates and the sigmoid router,
+ * and the layer's input gradient.
+ *   x [T, d] bf16, router_w [E, d] fp32     forward inputs
+ *   affinity [T, E] fp32                    the s the gates were made from
+ *                                           (moe_route's affinity_out)
+ *   topk_idx, row_of_slot, token_of_row, offsets   from moe_route
+ *   dgate [T, K] fp32                       from moe_combine_backward
+ *   dx_perm, dx_shared                      from moe_experts_backward_input
+ *   dlogit [T, K] fp32 out: dL/d(x . e) of every selected expert
+ *   dx [T, d] bf16 out: dL/dx of the layer input
+ *   drouter_w [E, d] fp32 out: dL/de (zero rows for unchosen experts)
+ *   ws, ws_bytes  the backward workspace (its last T*K*4 bytes)
+ */
+moe_status_t moe_route_backward(const moe_cfg_t* cfg, const void* x, const float* router_w,
+                                const float* affinity, const int32_t* topk_idx,
+                                const float* dgate, const int32_t* row_of_slot,
+                                const int32_t* token_of_row, const int32_t* offsets,
+                                const void* dx_perm, const void* dx_shared, float* dlogit,
+                                void* dx, float* drouter_w, void* ws, size_t ws_bytes,
+                                void* stream);
 
 /*
  * moe_quantize_weights_fp8 - offline utility: quantise `n_mats` bf16

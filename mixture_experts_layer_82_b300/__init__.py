@@ -40,7 +40,8 @@ EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_byt
             "moe_route", "moe_permute", "moe_experts_grouped", "moe_combine",
             "moe_bias_update", "moe_quantize_weights_fp8", "moe_get_device_error",
             "moe_route_static_scratch", "moe_experts_grouped_gather", "moe_balance_stat",
-            "moe_selftest_wait")
+            "moe_selftest_wait", "moe_backward_workspace_bytes", "moe_combine_backward",
+            "moe_experts_backward_input", "moe_experts_backward_weights", "moe_route_backward")
 
 
 class MoeCfg(ctypes.Structure):
@@ -93,6 +94,14 @@ _lib.moe_get_device_error.restype = ctypes.c_int
 _lib.moe_get_device_error.argtypes = [_P]
 _lib.moe_route_static_scratch.restype = ctypes.c_int
 _lib.moe_route_static_scratch.argtypes = [_CFG] + [_P] * 11 + [_P]
+
+
+_lib.moe_backward_workspace_bytes.restype = ctypes.c_size_t
+_lib.moe_backward_workspace_bytes.argtypes = [_CFG]
+_lib.moe_combine_backward.argtypes = [_CFG] + [_P] * 6 + [_P]
+_lib.moe_experts_backward_input.argtypes = [_CFG] + [_P] * 11 + [_P, ctypes.c_size_t, _P]
+_lib.moe_experts_backward_weights.argtypes = [_CFG] + [_P] * 9 + [_P, ctypes.c_size_t, _P]
+_lib.moe_route_backward.argtypes = [_CFG] + [_P] * 13 + [_P, ctypes.c_size_t, _P]
 
 
 def library():
@@ -278,6 +287,60 @@ def moe_bias_update(cfg, counts, bias, stream=None):
     _check("moe_bias_update", _lib.moe_bias_update(
         _cfg(cfg), _ptr(counts, "counts", torch.int32), _ptr(bias, "bias", torch.float32),
         _stream(stream)))
+
+
+# ---------------------------------------------------------------- backward
+_BF = torch.bfloat16
+
+
+def moe_backward_workspace_bytes(cfg):
+    return int(_lib.moe_backward_workspace_bytes(_cfg(cfg)))
+
+
+def moe_combine_backward(cfg, dout, y_perm, row_of_slot, topk_w, dy_perm, dgate, stream=None):
+    """dy_perm[row(t,k)] = g dout[t]; dgate[t,k] = dout[t] . y_perm[row(t,k)]."""
+    _check("moe_combine_backward", _lib.moe_combine_backward(
+        _cfg(cfg), _ptr(dout, "dout", _BF), _ptr(y_perm, "y_perm", _BF),
+        _ptr(row_of_slot, "row_of_slot", torch.int32), _ptr(topk_w, "topk_w", torch.float32),
+        _ptr(dy_perm, "dy_perm", _BF), _ptr(dgate, "dgate", torch.float32), _stream(stream)))
+
+
+def moe_experts_backward_input(cfg, x_perm, x, offsets, w13, w2, ws13, ws2, dy_perm, dout,
+                               dx_perm, dx_shared, ws, stream=None):
+    """Dgrad of the expert FFNs; leaves [da | db] and h in ws for the Wgrad."""
+    _check("moe_experts_backward_input", _lib.moe_experts_backward_input(
+        _cfg(cfg), _ptr(x_perm, "x_perm", _BF), _ptr(x, "x", _BF, allow_none=True),
+        _ptr(offsets, "offsets", torch.int32), _ptr(w13, "w13", _BF), _ptr(w2, "w2", _BF),
+        _ptr(ws13, "ws13", _BF, allow_none=True), _ptr(ws2, "ws2", _BF, allow_none=True),
+        _ptr(dy_perm, "dy_perm", _BF), _ptr(dout, "dout", _BF, allow_none=True),
+        _ptr(dx_perm, "dx_perm", _BF), _ptr(dx_shared, "dx_shared", _BF, allow_none=True),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_experts_backward_weights(cfg, x_perm, x, offsets, dy_perm, dout, dw13, dw2, dws13, dws2,
+                                 ws, stream=None):
+    """Wgrad of the expert FFNs from the intermediates the input call left in ws."""
+    _check("moe_experts_backward_weights", _lib.moe_experts_backward_weights(
+        _cfg(cfg), _ptr(x_perm, "x_perm", _BF), _ptr(x, "x", _BF, allow_none=True),
+        _ptr(offsets, "offsets", torch.int32), _ptr(dy_perm, "dy_perm", _BF),
+        _ptr(dout, "dout", _BF, allow_none=True), _ptr(dw13, "dw13", _BF),
+        _ptr(dw2, "dw2", _BF), _ptr(dws13, "dws13", _BF, allow_none=True),
+        _ptr(dws2, "dws2", _BF, allow_none=True),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_route_backward(cfg, x, router_w, affinity, topk_idx, dgate, row_of_slot, token_of_row,
+                       offsets, dx_perm, dx_shared, dlogit, dx, drouter_w, ws, stream=None):
+    """Gates -> logits -> router weights and the layer input gradient."""
+    _check("moe_route_backward", _lib.moe_route_backward(
+        _cfg(cfg), _ptr(x, "x", _BF), _ptr(router_w, "router_w", torch.float32),
+        _ptr(affinity, "affinity", torch.float32), _ptr(topk_idx, "topk_idx", torch.int32),
+        _ptr(dgate, "dgate", torch.float32), _ptr(row_of_slot, "row_of_slot", torch.int32),
+        _ptr(token_of_row, "token_of_row", torch.int32), _ptr(offsets, "offsets", torch.int32),
+        _ptr(dx_perm, "dx_perm", _BF), _ptr(dx_shared, "dx_shared", _BF, allow_none=True),
+        _ptr(dlogit, "dlogit", torch.float32), _ptr(dx, "dx", _BF),
+        _ptr(drouter_w, "drouter_w", torch.float32),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_quantize_weights_fp8(w, q, scales, stream=None):

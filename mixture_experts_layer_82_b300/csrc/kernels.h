@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -88,6 +89,60 @@ void experts_scratch_carve(const moe_cfg_t& c, void* ws, void** h, float** h_sca
 cudaError_t launch_experts_fp32(const ExpertsArgs& a, cudaStream_t s);
 cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t s);
 cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t s);
+
+// backward (BF16 kind)
+struct ExpertsBwdScratch {
+  __nv_bfloat16* ab;         // [T*K, 2I]: [a | b], then [da | db]
+  __nv_bfloat16* ab_shared;  // [T, N_s * 2I]: per shared expert [a | b], then [da | db]
+  __nv_bfloat16* h;          // [T*K, I]
+  __nv_bfloat16* h_shared;   // [T, N_s * I]
+};
+
+struct ExpertsBwdArgs {
+  const moe_cfg_t* cfg;
+  const void* x_perm;
+  const void* x;
+  const int32_t* offsets;
+  const void* w13;
+  const void* w2;
+  const void* ws13;
+  const void* ws2;
+  const void* dy_perm;
+  const void* dout;
+  void* dx_perm;
+  void* dx_shared;
+  void* dw13;
+  void* dw2;
+  void* dws13;
+  void* dws2;
+  ExpertsBwdScratch scratch;
+};
+
+struct RouteBwdArgs {
+  const void* x;
+  const float* router_w;
+  const float* affinity;
+  const int32_t* topk_idx;
+  const float* dgate;
+  const int32_t* row_of_slot;
+  const int32_t* token_of_row;
+  const int32_t* offsets;
+  const void* dx_perm;
+  const void* dx_shared;
+  float* dlogit;
+  float* dlogit_row;  // scratch [T*K]
+  void* dx;
+  float* drouter_w;
+};
+
+size_t experts_bwd_scratch_bytes(const moe_cfg_t& c);
+ExpertsBwdScratch experts_bwd_scratch_carve(const moe_cfg_t& c, void* ws);
+cudaError_t launch_experts_bwd_input_bf16(const ExpertsBwdArgs& a, cudaStream_t s);
+cudaError_t launch_experts_bwd_weights_bf16(const ExpertsBwdArgs& a, cudaStream_t s);
+cudaError_t launch_combine_backward(const moe_cfg_t& c, const void* dout, const void* y_perm,
+                                    const int32_t* row_of_slot, const float* topk_w,
+                                    void* dy_perm, float* dgate, cudaStream_t s);
+cudaError_t launch_route_backward(const moe_cfg_t& c, const RouteBwdArgs& a, cudaStream_t s);
 
 // Driver entry point of cuTensorMapEncodeTiled (resolved once).
 CUresult encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, void* base,

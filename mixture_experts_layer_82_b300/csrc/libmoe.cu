@@ -7,5 +7,7 @@
 #include "experts_fp32.cu"
 #include "experts_sm100.cu"
 #include "experts_fp8.cu"
+#include "backward_sm100.cu"
+#include "backward.cu"
 #include "tma.cu"
 #include "route_static.cu"

@@ -268,6 +268,132 @@ moe_status_t moe_balance_stat(const moe_cfg_t* cfg, const float* affinity,
                                        loss_out, ws, as_stream(stream)));
 }
 
+// ------------------------------------------------------------ backward pass
+namespace {
+
+moe_status_t check_backward_cfg(const moe_cfg_t* cfg) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->dtype != MOE_DTYPE_BF16 || cfg->n_shared > 64) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+size_t backward_route_bytes(const moe_cfg_t& c) {
+  return align_up(static_cast<size_t>(c.T) * c.K * 4, 256);
+}
+
+}  // namespace
+
+size_t moe_backward_workspace_bytes(const moe_cfg_t* c) {
+  if (check_backward_cfg(c) != MOE_OK) return 0;
+  return experts_bwd_scratch_bytes(*c) + backward_route_bytes(*c);
+}
+
+moe_status_t moe_combine_backward(const moe_cfg_t* cfg, const void* dout, const void* y_perm,
+                                  const int32_t* row_of_slot, const float* topk_w,
+                                  void* dy_perm, float* dgate, void* stream) {
+  moe_status_t st = check_backward_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (dout == nullptr || y_perm == nullptr || row_of_slot == nullptr || topk_w == nullptr ||
+      dy_perm == nullptr || dgate == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {dout, y_perm, row_of_slot, topk_w, dy_perm, dgate};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  return from_cuda(launch_combine_backward(*cfg, dout, y_perm, row_of_slot, topk_w, dy_perm,
+                                           dgate, as_stream(stream)));
+}
+
+moe_status_t moe_experts_backward_input(const moe_cfg_t* cfg, const void* x_perm,
+                                        const void* x, const int32_t* offsets, const void* w13,
+                                        const void* w2, const void* ws13, const void* ws2,
+                                        const void* dy_perm, const void* dout, void* dx_perm,
+                                        void* dx_shared, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  moe_status_t st = check_backward_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (x_perm == nullptr || offsets == nullptr || w13 == nullptr || w2 == nullptr ||
+      dy_perm == nullptr || dx_perm == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0 && (x == nullptr || ws13 == nullptr || ws2 == nullptr || dout == nullptr ||
+                         dx_shared == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_perm, x, offsets, w13, w2, ws13, ws2, dy_perm, dout, dx_perm,
+                        dx_shared, ws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_backward_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  ExpertsBwdArgs a{};
+  a.cfg = &c;
+  a.x_perm = x_perm; a.x = x; a.offsets = offsets;
+  a.w13 = w13; a.w2 = w2; a.ws13 = ws13; a.ws2 = ws2;
+  a.dy_perm = dy_perm; a.dout = dout;
+  a.dx_perm = dx_perm; a.dx_shared = c.n_shared > 0 ? dx_shared : nullptr;
+  a.scratch = experts_bwd_scratch_carve(c, ws);
+  return from_cuda(launch_experts_bwd_input_bf16(a, as_stream(stream)));
+}
+
+moe_status_t moe_experts_backward_weights(const moe_cfg_t* cfg, const void* x_perm,
+                                          const void* x, const int32_t* offsets,
+                                          const void* dy_perm, const void* dout, void* dw13,
+                                          void* dw2, void* dws13, void* dws2, void* ws,
+                                          size_t ws_bytes, void* stream) {
+  moe_status_t st = check_backward_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (x_perm == nullptr || offsets == nullptr || dy_perm == nullptr || dw13 == nullptr ||
+      dw2 == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0 && (x == nullptr || dout == nullptr || dws13 == nullptr || dws2 == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_perm, x, offsets, dy_perm, dout, dw13, dw2, dws13, dws2, ws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_backward_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  ExpertsBwdArgs a{};
+  a.cfg = &c;
+  a.x_perm = x_perm; a.x = x; a.offsets = offsets;
+  a.dy_perm = dy_perm; a.dout = dout;
+  a.dw13 = dw13; a.dw2 = dw2;
+  a.dws13 = c.n_shared > 0 ? dws13 : nullptr;
+  a.dws2 = c.n_shared > 0 ? dws2 : nullptr;
+  a.scratch = experts_bwd_scratch_carve(c, ws);
+  return from_cuda(launch_experts_bwd_weights_bf16(a, as_stream(stream)));
+}
+
+moe_status_t moe_route_backward(const moe_cfg_t* cfg, const void* x, const float* router_w,
+                                const float* affinity, const int32_t* topk_idx,
+                                const float* dgate, const int32_t* row_of_slot,
+                                const int32_t* token_of_row, const int32_t* offsets,
+                                const void* dx_perm, const void* dx_shared, float* dlogit,
+                                void* dx, float* drouter_w, void* ws, size_t ws_bytes,
+                                void* stream) {
+  moe_status_t st = check_backward_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (x == nullptr || router_w == nullptr || affinity == nullptr || topk_idx == nullptr ||
+      dgate == nullptr || row_of_slot == nullptr || token_of_row == nullptr ||
+      offsets == nullptr || dx_perm == nullptr || dlogit == nullptr || dx == nullptr ||
+      drouter_w == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0 && dx_shared == nullptr) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, router_w, affinity, topk_idx, dgate, row_of_slot, token_of_row,
+                        offsets, dx_perm, dx_shared, dlogit, dx, drouter_w, ws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_backward_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  RouteBwdArgs a{};
+  a.x = x; a.router_w = router_w; a.affinity = affinity; a.topk_idx = topk_idx;
+  a.dgate = dgate; a.row_of_slot = row_of_slot; a.token_of_row = token_of_row;
+  a.offsets = offsets; a.dx_perm = dx_perm;
+  a.dx_shared = c.n_shared > 0 ? dx_shared : nullptr;
+  a.dlogit = dlogit;
+  a.dlogit_row = reinterpret_cast<float*>(static_cast<char*>(ws) + experts_bwd_scratch_bytes(c));
+  a.dx = dx; a.drouter_w = drouter_w;
+  return from_cuda(launch_route_backward(c, a, as_stream(stream)));
+}
+
 moe_status_t moe_quantize_weights_fp8(const void* w_bf16, int32_t n_mats, int32_t rows,
                                       int32_t cols, void* q, float* scales, void* stream) {
   if (w_bf16 == nullptr || q == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;

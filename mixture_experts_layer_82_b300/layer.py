@@ -1,13 +1,16 @@
 """One DeepSeekMoE layer: the buffers of a batch and the five library calls
 of a forward step (route -> permute -> experts -> combine -> bias update),
-enqueued on one stream with no host synchronisation."""
+enqueued on one stream with no host synchronisation; for the bf16 kind also
+the four calls of its backward pass."""
 
 from __future__ import annotations
 
 import torch
 
 from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_experts_grouped_gather,
-               moe_combine, moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes)
+               moe_combine, moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes,
+               moe_backward_workspace_bytes, moe_combine_backward, moe_experts_backward_input,
+               moe_experts_backward_weights, moe_route_backward)
 
 
 def _quantize(w, stream=None):
@@ -104,3 +107,53 @@ class MoELayer:
         if update_bias:
             moe_bias_update(c, self.counts, self.bias, stream=stream)
         return out
+
+    # ------------------------------------------------------------- backward
+    def _grad_buffers(self):
+        c = self.cfg
+        dev = self.router_w.device
+        T, d, E, K, I, ns = c.T, c.d, c.E, c.k, c.inter, c.n_shared
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.dy_perm = torch.empty(T * K, d, **bf)
+        self.dgate = torch.empty(T, K, **f32)
+        self.dx_perm = torch.empty(T * K, d, **bf)
+        self.dx_shared = torch.empty(T, d, **bf) if ns else None
+        self.dlogit = torch.empty(T, K, **f32)
+        self.dx = torch.empty(T, d, **bf)
+        self.drouter_w = torch.empty(E, d, **f32)
+        self.dw13 = torch.empty(E, 2 * I, d, **bf)
+        self.dw2 = torch.empty(E, d, I, **bf)
+        self.dws13 = torch.empty(ns, 2 * I, d, **bf) if ns else None
+        self.dws2 = torch.empty(ns, d, I, **bf) if ns else None
+        self.bws = torch.empty(moe_backward_workspace_bytes(c), dtype=torch.uint8, device=dev)
+
+    def backward(self, x, dout, affinity, stream=None, weights=True):
+        """Backward of the last ``forward(x, affinity_out=affinity)`` (bf16
+        kind), given ``dout`` = dL/dy [T, d] bf16.  Fills ``dx``,
+        ``drouter_w`` and, with ``weights``, ``dw13``, ``dw2``, ``dws13``,
+        ``dws2`` (plus the intermediates ``dy_perm``, ``dgate``, ``dlogit``,
+        ``dx_perm``, ``dx_shared``); returns ``dx``.  The selection and the
+        bias are those of the forward; the bias gets no gradient."""
+        c = self.cfg
+        if c.dtype != "bf16":
+            raise ValueError("the backward pass is implemented for the bf16 kind")
+        if not hasattr(self, "bws"):
+            self._grad_buffers()
+        if self.gather:
+            # the gathering forward never wrote the permuted rows
+            moe_permute(c, x, self.token_of_row, self.x_perm, stream=stream)
+        moe_combine_backward(c, dout, self.y_perm, self.row_of_slot, self.topk_w, self.dy_perm,
+                             self.dgate, stream=stream)
+        moe_experts_backward_input(c, self.x_perm, x, self.offsets, self.w13, self.w2, self.ws13,
+                                   self.ws2, self.dy_perm, dout, self.dx_perm, self.dx_shared,
+                                   self.bws, stream=stream)
+        moe_route_backward(c, x, self.router_w, affinity, self.topk_idx, self.dgate,
+                           self.row_of_slot, self.token_of_row, self.offsets, self.dx_perm,
+                           self.dx_shared, self.dlogit, self.dx, self.drouter_w, self.bws,
+                           stream=stream)
+        if weights:
+            moe_experts_backward_weights(c, self.x_perm, x, self.offsets, self.dy_perm, dout,
+                                         self.dw13, self.dw2, self.dws13, self.dws2, self.bws,
+                                         stream=stream)
+        return self.dx

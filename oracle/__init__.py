@@ -48,5 +48,8 @@ from .moe_fp8 import (  # noqa: F401
 from .moe_backward import (  # noqa: F401
     swiglu_ffn_backward,
     gate_backward,
+    combine_backward,
+    input_grad,
+    router_weight_grad,
     moe_layer_backward,
 )

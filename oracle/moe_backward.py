@@ -89,6 +89,55 @@ def gate_backward(s_sel, idx, route_scale, dgate):
     return ds, ds * s * (1.0 - s)
 
 
+def combine_backward(dout, y_perm, row_of_slot, gates):
+    """Gradient of the gate-weighted combine.  For every slot (t, j), with
+    r = row_of_slot[t, j]: the routed row's gradient dy_slot[t, j] =
+    g[t, j] dout[t] (it belongs at permuted row r) and
+    dgate[t, j] = dout[t] . y_perm[r].  ``y_perm`` may hold only the rows the
+    slots name (any indexable).  Returns (dy_slot [T, K, d], dgate [T, K])."""
+    dout = np.asarray(dout, dtype=np.float64)
+    ros = np.asarray(row_of_slot, dtype=np.int64)
+    gates = np.asarray(gates, dtype=np.float64)
+    T, K = ros.shape
+    dy_slot = np.zeros((T, K, dout.shape[1]))
+    dgate = np.zeros((T, K))
+    for t in range(T):
+        for j in range(K):
+            dgate[t, j] = float(np.dot(dout[t], np.asarray(y_perm[ros[t, j]], dtype=np.float64)))
+            dy_slot[t, j] = gates[t, j] * dout[t]
+    return dy_slot, dgate
+
+
+def input_grad(dx_shared, dx_perm, row_of_slot, idx, dlogit, router_w):
+    """dL/dx_t = dx_shared[t] + sum_j (dx_perm[row_of_slot[t, j]]
+    + dlogit[t, j] e_{idx[t, j]}): the shared experts, the routed experts'
+    input gradients brought back to their token, and the router's share
+    through the logits l = x . e."""
+    ros = np.asarray(row_of_slot, dtype=np.int64)
+    idx = np.asarray(idx, dtype=np.int64)
+    T, K = ros.shape
+    rw = np.asarray(router_w, dtype=np.float64)
+    d = rw.shape[1]
+    dx = np.zeros((T, d)) if dx_shared is None else np.array(dx_shared, dtype=np.float64)
+    for t in range(T):
+        for j in range(K):
+            dx[t] += np.asarray(dx_perm[ros[t, j]], dtype=np.float64) + dlogit[t, j] * rw[idx[t, j]]
+    return dx
+
+
+def router_weight_grad(x, idx, dlogit, n_experts):
+    """dL/de_i = sum over the slots (t, j) with idx[t, j] = i of
+    dlogit[t, j] x_t (unchosen experts get zero rows)."""
+    x = np.asarray(x, dtype=np.float64)
+    idx = np.asarray(idx, dtype=np.int64)
+    T, K = idx.shape
+    g = np.zeros((n_experts, x.shape[1]))
+    for t in range(T):
+        for j in range(K):
+            g[idx[t, j]] += dlogit[t, j] * x[t]
+    return g
+
+
 def moe_layer_backward(x, router_w, w13, w2, ws13, ws2, fwd, dout, *, route_scale=1.0,
                        affinity32=None, y_perm=None):
     """Backward of one DeepSeekMoE layer in fp64, selection held fixed.
@@ -122,11 +171,10 @@ def moe_layer_backward(x, router_w, w13, w2, ws13, ws2, fwd, dout, *, route_scal
              else np.asarray(affinity32, dtype=np.float32))
 
     # combine: out[t] = y_shared[t] + sum_j g[t, j] y_perm[row_of_slot[t, j]]
-    dgate = np.zeros((T, K))
+    dy_slot, dgate = combine_backward(dout, yp, ros, gates)
     dy_perm = np.zeros((T * K, d))
     for j in range(K):
-        dgate[:, j] = (dout * yp[ros[:, j]]).sum(axis=1)
-        dy_perm[ros[:, j]] = gates[:, j:j + 1] * dout
+        dy_perm[ros[:, j]] = dy_slot[:, j]
 
     # routed experts, one segment at a time
     x_perm = permute_rows(x64, fwd["token_of_row"])
@@ -164,12 +212,8 @@ def moe_layer_backward(x, router_w, w13, w2, ws13, ws2, fwd, dout, *, route_scal
 
     # gates -> logits -> router weights and input
     _, dlogit = gate_backward(s_sel, idx, route_scale, dgate)
-    dx = np.zeros((T, d)) if dx_shared is None else dx_shared.copy()
-    drouter_w = np.zeros((E, d))
-    for t in range(T):
-        for j in range(K):
-            dx[t] += dx_perm[ros[t, j]] + dlogit[t, j] * rw[idx[t, j]]
-            drouter_w[idx[t, j]] += dlogit[t, j] * x64[t]
+    dx = input_grad(dx_shared, dx_perm, ros, idx, dlogit, rw)
+    drouter_w = router_weight_grad(x64, idx, dlogit, E)
     return {
         "dy_perm": dy_perm, "dgate": dgate, "dlogit": dlogit, "dx_perm": dx_perm,
         "dx_shared": dx_shared, "dx": dx, "drouter_w": drouter_w, "dw13": dw13,
