@@ -12,6 +12,10 @@ groups, top-4 groups, top-8, 1 shared expert, I=2048, route scale 2.5, Zipf
 its own batch (weak scaling, no collective on the data path); the time is
 the maximum over ranks.  Rank 0 prints one JSON line.
 
+``--train`` (bf16 kind) makes a step one training pass instead: the forward
+above, then its backward (combine backward, expert Dgrad with the gate/up
+products recomputed, router backward, expert Wgrad), given a fixed dL/dy.
+
 ``--impl reference`` times the CPU oracle (fp64 NumPy) on the host cores on a
 bounded sample of the same workload; that is the only other place, besides
 the ``cpu_baseline`` leg, where this script runs the oracle.
@@ -38,6 +42,8 @@ sys.path.insert(0, ROOT)
 from moe_synth import CONFIGS, make_layer  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at V3 shape (bf16, FP8); TFLOP/s as % of B300 peak"
+METRIC_TRAIN = ("MoE-layer training tokens/s (forward + backward) at V3 shape (bf16); "
+                "TFLOP/s as % of B300 peak")
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL_SRC = {"bf16": "mixture_experts_layer_82_b300/csrc/experts_sm100.cu",
               "fp8": "mixture_experts_layer_82_b300/csrc/experts_fp8.cu"}
@@ -71,6 +77,22 @@ def expert_bytes(shape, counts):
            + 2 * (rows + shape.T * shape.n_shared) * shape.inter * ab
            + (rows + shape.T * (1 if shape.n_shared else 0)) * shape.d * ab)
     return weights + act, touched
+
+
+def backward_flops(shape):
+    """Algorithmic FLOPs of the expert backward: Dgrad (dh = dy W2 and
+    dx = [da | db] W13) and Wgrad (dW2 and dW13), 6 d I per row each.  The
+    recomputation of [a | b] (4 d I per row) is not counted."""
+    rows = shape.T * shape.k + shape.T * shape.n_shared
+    return {"dgrad": 6.0 * shape.d * shape.inter * rows, "wgrad": 6.0 * shape.d * shape.inter * rows,
+            "recompute": 4.0 * shape.d * shape.inter * rows}
+
+
+def train_launches(shape, gather=False):
+    """Kernels of one training step: the forward's, then combine backward,
+    the recompute, two Dgrad and two Wgrad GEMMs, the router backward's two
+    kernels, and a permute when the forward gathered its rows."""
+    return launches_per_step(shape, gather) + 1 + 1 + 2 + 2 + 2 + (1 if gather else 0)
 
 
 def layer_flops(shape):
@@ -305,6 +327,39 @@ def oracle_sample(shape, L, n_tokens, token0=0):
     return time.perf_counter() - t0, n_tokens
 
 
+def oracle_train_sample(shape, L, n_tokens, token0=0):
+    """The fp64 oracle forward + backward on n_tokens tokens of the workload
+    taken as a batch of their own (their routing, expert and router
+    gradients); returns (seconds, tokens)."""
+    import oracle
+    from moe_synth import make_grad
+
+    class View:
+        def __init__(self, t):
+            self.t = t
+
+        def __len__(self):
+            return self.t.shape[0]
+
+        def __getitem__(self, e):
+            return self.t[e].float().cpu().numpy()
+
+    rows = torch.arange(token0, token0 + n_tokens, device=L["x"].device)
+    x = L["x"][rows].float().cpu().numpy()
+    go = make_grad(shape, L["x"].device)[rows].float().cpu().numpy()
+    rw = L["router_w"].cpu().numpy()
+    b = L["bias"].cpu().numpy()
+    ws13 = View(L["ws13"]) if shape.n_shared else None
+    ws2 = View(L["ws2"]) if shape.n_shared else None
+    t0 = time.perf_counter()
+    fwd = oracle.moe_layer_forward(x, rw, b, View(L["w13"]), View(L["w2"]), ws13, ws2,
+                                   n_groups=shape.n_groups, topk_groups=shape.topk_groups,
+                                   k=shape.k, route_scale=shape.route_scale)
+    oracle.moe_layer_backward(x, rw, View(L["w13"]), View(L["w2"]), ws13, ws2, fwd, go,
+                              route_scale=shape.route_scale)
+    return time.perf_counter() - t0, n_tokens
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -323,20 +378,23 @@ def run_reference(args, shape, world, rank):
         return 0
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     L = make_layer(shape, dev)
+    fn = oracle_train_sample if args.train else oracle_sample
     for i in range(args.warmup):
-        oracle_sample(shape, L, args.ref_tokens, token0=i * args.ref_tokens)
+        fn(shape, L, args.ref_tokens, token0=i * args.ref_tokens)
     secs, toks = 0.0, 0
     for i in range(args.steps):
-        s, n = oracle_sample(shape, L, args.ref_tokens,
-                             token0=((args.warmup + i) * args.ref_tokens) % (shape.T - args.ref_tokens))
+        s, n = fn(shape, L, args.ref_tokens,
+                  token0=((args.warmup + i) * args.ref_tokens) % (shape.T - args.ref_tokens))
         secs += s
         toks += n
     value = toks / secs
     cores = blas_threads()
     sample = (f"{args.ref_tokens} tokens of the {shape.name} batch per step, end to end "
               f"(affinity, group-limited top-k, gates, shared + routed SwiGLU experts in fp64, "
-              f"combine); expert weights fetched from device memory per expert")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+              f"combine{'; then the whole backward' if args.train else ''}); expert weights "
+              f"fetched from device memory per expert")
+    line = {"impl": "reference", "metric": METRIC_TRAIN if args.train else METRIC,
+            "value": value, "unit": "tokens/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -521,6 +579,137 @@ def run_ours(args, shape, world, rank, local):
     return 0
 
 
+def run_train(args, shape, world, rank, local):
+    """One training step per iteration: forward (with the bias update) and
+    the whole backward, inputs and dL/dy resident on the device."""
+    import mixture_experts_layer_82_b300 as moe
+    from moe_synth import make_grad
+
+    if shape.dtype != "bf16":
+        raise SystemExit("--train: the backward pass is implemented for the bf16 kind")
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    L = make_layer(shape, dev)
+    cfg = moe.LayerCfg.from_shape(shape)
+    gather = args.dispatch == "gather"
+    layer = moe.MoELayer(cfg, L["router_w"], L["bias"].clone(), L["w13"], L["w2"],
+                         L["ws13"] if shape.n_shared else None, L["ws2"] if shape.n_shared else None,
+                         gather=gather)
+    x = L["x"]
+    dout = make_grad(shape, dev)
+    aff = torch.empty(shape.T, shape.E, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(xx, gg, ev=None):
+        layer.forward(xx, affinity_out=aff, expert_events=None if ev is None else ev[0:2])
+        return layer.backward(xx, gg, aff, events=None if ev is None else ev[2:6])
+
+    for _ in range(args.warmup):
+        step(x, dout)
+    torch.cuda.synchronize()
+    if moe.moe_get_device_error() != 0:
+        raise RuntimeError("device error after warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        step(x, dout, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    parts = {"forward experts": [e[0].elapsed_time(e[1]) for e in evs],
+             "backward experts, input (Dgrad + recompute)": [e[2].elapsed_time(e[3]) for e in evs],
+             "backward experts, weights (Wgrad)": [e[4].elapsed_time(e[5]) for e in evs]}
+    if moe.moe_get_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+
+    # ---- end to end: x and dL/dy from pinned host memory, dL/dx back, every
+    # step, on the compute stream (no overlap)
+    x_host = x.cpu().pin_memory()
+    g_host = dout.cpu().pin_memory()
+    dx_host = torch.empty(shape.T, shape.d, dtype=torch.bfloat16).pin_memory()
+    x_dev, g_dev = torch.empty_like(x), torch.empty_like(dout)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        g_dev.copy_(g_host, non_blocking=True)
+        dx_host.copy_(step(x_dev, g_dev), non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    if moe.moe_get_device_error() != 0:
+        raise RuntimeError("device error in the end-to-end region")
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops"]
+    peak_sust = peaks.get("bf16_tflops_sustained", peak)
+    bf = backward_flops(shape)
+    alg = {"forward experts": expert_flops(shape),
+           "backward experts, input (Dgrad + recompute)": bf["dgrad"],
+           "backward experts, weights (Wgrad)": bf["wgrad"]}
+    breakdown = {}
+    for k, v in parts.items():
+        m = statistics.mean(v)
+        breakdown[k] = {"ms_per_step": m, "algorithmic_tflop": alg[k] / 1e12,
+                        "tflops": alg[k] / (m * 1e-3) / 1e12}
+    dom = max(breakdown, key=lambda k: breakdown[k]["ms_per_step"])
+    achieved = breakdown[dom]["tflops"]
+    tokens = world * shape.T * K
+    # expert forward, Dgrad and Wgrad, and the dense router product; the
+    # router backward touches only the K selected centroids (4 T K d, small)
+    step_flops = expert_flops(shape) + bf["dgrad"] + bf["wgrad"] + 2.0 * shape.T * shape.d * shape.E
+    line = {
+        "metric": METRIC_TRAIN, "value": tokens / (total_ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": describe(shape), "global_batch": world * shape.T,
+                   "step": "forward (route, permute, experts, combine, bias update) + backward "
+                           "(combine, experts Dgrad with [a|b] recomputed, router, experts Wgrad)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: every step streams all expert weights and "
+                         "writes all weight gradients"},
+        "layer_tflops": step_flops * world * K / (total_ms * 1e-3) / 1e12,
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_kind": f"bf16 dense burst, {peaks['_source']}",
+                     "frac_of_sustained": achieved / peak_sust, "traffic": None,
+                     "breakdown": breakdown,
+                     "recompute_tflop_not_counted": bf["recompute"] / 1e12},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": dx_host.numel() * dx_host.element_size(),
+                "copies": "x and dL/dy in, dL/dx out, on the compute stream"},
+        "gpu_launches": train_launches(shape, gather) * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, n = oracle_train_sample(shape, L, args.cpu_tokens)
+        line["cpu_baseline"] = {
+            "value": n / secs, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} tokens of the same batch through the fp64 oracle forward and "
+                      f"backward ({secs:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -534,6 +723,8 @@ def main():
     ap.add_argument("--dispatch", choices=["permute", "gather"], default="permute",
                     help="bf16 kind: permute x into per-expert rows before the expert GEMMs, "
                          "or gather the rows inside the gate/up GEMM")
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step (forward + backward; bf16 kind)")
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                     help="override a field of the workload's shape (a reduced case for "
                          "profiling, e.g. --set E=32 --set router=gaussian)")
@@ -557,6 +748,8 @@ def main():
     try:
         if args.impl == "reference":
             return run_reference(args, shape, world, rank)
+        if args.train:
+            return run_train(args, shape, world, rank, local)
         return run_ours(args, shape, world, rank, local)
     finally:
         if world > 1:

@@ -23,11 +23,12 @@
 //   DG_PLAIN   dx tile = [da | db] rows x W13 (A K-major, B MN-major)
 //   WG         dW tile = A^T B over the rows of one segment (both
 //              MN-major); K is the segment length, so the last K block is
-//              ragged: its rows past the segment are zeroed in shared memory
+//              ragged: A's rows past the segment are zeroed in shared memory
 //              before the MMAs read them
 // The work list is every (group, M tile, N tile); groups are the E routed
 // experts, then the shared experts.  Inside a group the M tile varies
-// fastest.  Roles, barriers, bounded waits and the abort path are those of
+// fastest for Dgrad (the CTAs running together share a weight tile through
+// L2) and the N tile for Wgrad (they write whole row bands of the gradient).  Roles, barriers, bounded waits and the abort path are those of
 // the forward grouped GEMM (experts_sm100.cu): warps 0 and 6 produce, warp 1
 // issues MMAs into two 256-column fp32 accumulators, warps 2..5 drain them.
 #include <algorithm>
@@ -48,6 +49,7 @@ constexpr int THREADS = 224;
 constexpr int PRODUCER2 = 6;
 constexpr int MAX_GROUPS = 1025 + 64;  // routed experts + shared experts
 constexpr uint32_t TMEM_COLS = 512;
+static_assert(BN == 256, "the Wgrad epilogue drains an accumulator as four 64-column chunks");
 
 enum Kind { DG_SWIGLU = 0, DG_PLAIN = 1, WG = 2 };
 
@@ -82,6 +84,9 @@ struct Params {
 };
 
 struct Smem {
+  // Wgrad epilogue: per epilogue warp, 32 rows x 64 bf16 columns (128-byte
+  // rows, 16-byte pieces XOR-swizzled by the row) on their way to global
+  alignas(16) uint8_t stage_out[4][32 * 128];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tfull[2];
@@ -151,6 +156,7 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
   }
 }
 
+template <int KIND>
 __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int t) {
   int lo = 0, hi = s.n_groups;
   while (hi - lo > 1) {
@@ -161,9 +167,18 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int 
   tl.cls = lo < p.E ? 0 : 1;
   tl.j = tl.cls == 0 ? lo : lo - p.E;
   const int local = t - s.gstart[lo];
-  const int mt_count = s.mtiles[lo];
-  tl.mt = local % mt_count;
-  tl.nt = local / mt_count;
+  if (KIND == WG) {
+    // N tile fastest: the CTAs of a wave write whole row bands of the
+    // gradient matrix (long contiguous runs in DRAM)
+    const int nt_count = tiles_n<KIND>(p);
+    tl.nt = local % nt_count;
+    tl.mt = local / nt_count;
+  } else {
+    // M tile fastest: the CTAs of a wave share one weight tile through L2
+    const int mt_count = s.mtiles[lo];
+    tl.mt = local % mt_count;
+    tl.nt = local / mt_count;
+  }
   if (tl.cls == 0) { tl.row0 = s.off[lo]; tl.rows = max(s.off[lo + 1] - tl.row0, 0); }
   else { tl.row0 = 0; tl.rows = p.T; }
   return tl;
@@ -235,7 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
       uint32_t g = 0, mine = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < total && !stop && !*abort_flag; t += gridDim.x) {
-        const Tile tl = decode_tile(p, s, t);
+        const Tile tl = decode_tile<KIND>(p, s, t);
         const ClassDesc& cd = p.cls[tl.cls];
         const int nk = k_blocks<KIND>(p, tl);
         const CUtensorMap* am = &p.a_map[tl.cls];
@@ -284,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
     int it = 0;
     bool any = false;
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++it) {
-      const Tile tl = decode_tile(p, s, t);
+      const Tile tl = decode_tile<KIND>(p, s, t);
       const int nk = k_blocks<KIND>(p, tl);
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
@@ -304,13 +319,16 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
         if (KIND == WG) {
           const int valid = min(tl.rows - kb * BK, BK);
           if (valid < BK) {
-            const int per_box = (BK - valid) * 8;  // 16-byte chunks past the segment
-            for (int i = lane; i < (BM / 64 + BN / 64) * per_box; i += 32) {
-              const int box = i / per_box, c = i % per_box;
-              uint8_t* base = box < BM / 64 ? sa + box * BOX_BYTES
-                                            : sb + (box - BM / 64) * BOX_BYTES;
-              *reinterpret_cast<uint4*>(base + valid * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-            }
+            // Zero A's K rows past the segment (16-byte chunks from line
+            // `valid` to the end of both A boxes): their products with B
+            // vanish whatever B holds there, as long as it is finite (B's
+            // rows past a segment are rows of the next segment, written by
+            // the library, or TMA's zero fill past the end of the tensor).
+            const uint32_t from = static_cast<uint32_t>(valid) * 128u + lane * 16u;
+#pragma unroll
+            for (int box = 0; box < BM / 64; ++box)
+              for (uint32_t o = from; o < static_cast<uint32_t>(BOX_BYTES); o += 512u)
+                *reinterpret_cast<uint4*>(sa + box * BOX_BYTES + o) = make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
           }
           __syncwarp();
@@ -346,7 +364,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
     const int r_in_tile = q * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const Tile tl = decode_tile(p, s, t);
+      const Tile tl = decode_tile<KIND>(p, s, t);
       const ClassDesc& cd = p.cls[tl.cls];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
@@ -356,29 +374,61 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
                              (static_cast<uint32_t>(q * 32) << 16);
       const int n_base = tl.nt * BN;
       if (KIND == WG) {
-        const int m = tl.mt * BM + r_in_tile;
-        const bool valid = m < p.m_dim;
+        // The weight-gradient tile is written whole (64 KiB per tile, about
+        // as much time as its MMAs take), so the stores are coalesced: per
+        // 64-column chunk each lane puts its row into the warp's staging
+        // rows (16-byte pieces XOR-swizzled by the row), then the warp
+        // writes 4 full 128-byte rows per store instruction.  The TMEM
+        // loads of the next chunk are in flight meanwhile.  m_dim is a
+        // multiple of 128, so every row is inside the matrix.
         const bool empty = tl.rows == 0;
-        __nv_bfloat16* orow = cd.out + cd.out_group_stride * tl.j +
-                              static_cast<size_t>(valid ? m : 0) * p.n_dim + n_base;
-#pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          float v[16];
-          if (!empty) {
-            tmem_ld16(taddr + c * 16, v);
-            tmem_ld_wait();
-          } else {
+        uint8_t* stg = s.stage_out[q];
+        __nv_bfloat16* obase = cd.out + cd.out_group_stride * tl.j +
+                               static_cast<size_t>(tl.mt * BM + q * 32) * p.n_dim;
+        const int cc = lane & 7;
+        auto put = [&](const float (&x0)[32], const float (&x1)[32], int c) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int j = 0; j < 8; ++j) {
+            const float* x = j < 4 ? x0 + 8 * j : x1 + 8 * (j - 4);
+            const uint4 w = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                                       pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
           }
-          uint32_t pk[8];
+          __syncwarp();
+          const int col = n_base + c * 64 + cc * 8;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-          if (valid && n_base + c * 16 < p.n_dim) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + (lane >> 3);
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((cc ^ (rr & 7)) << 4));
+            if (col < p.n_dim)
+              *reinterpret_cast<uint4*>(obase + static_cast<size_t>(rr) * p.n_dim + col) = w;
           }
+          __syncwarp();
+        };
+        float a0[32], a1[32], b0[32], b1[32];
+        if (empty) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a0[i] = a1[i] = 0.f;
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) put(a0, a1, c);
+        } else {
+          // chunk c + 1's TMEM loads are in flight while chunk c is stored
+          tmem_ld32(taddr, a0);
+          tmem_ld32(taddr + 32, a1);
+          tmem_ld_wait();
+          tmem_ld32(taddr + 64, b0);
+          tmem_ld32(taddr + 96, b1);
+          put(a0, a1, 0);
+          tmem_ld_wait();
+          tmem_ld32(taddr + 128, a0);
+          tmem_ld32(taddr + 160, a1);
+          put(b0, b1, 1);
+          tmem_ld_wait();
+          tmem_ld32(taddr + 192, b0);
+          tmem_ld32(taddr + 224, b1);
+          put(a0, a1, 2);
+          tmem_ld_wait();
+          put(b0, b1, 3);
         }
       } else {
         const int m = tl.mt * BM + r_in_tile;

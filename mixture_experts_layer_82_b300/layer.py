@@ -128,13 +128,15 @@ class MoELayer:
         self.dws2 = torch.empty(ns, d, I, **bf) if ns else None
         self.bws = torch.empty(moe_backward_workspace_bytes(c), dtype=torch.uint8, device=dev)
 
-    def backward(self, x, dout, affinity, stream=None, weights=True):
+    def backward(self, x, dout, affinity, stream=None, weights=True, events=None):
         """Backward of the last ``forward(x, affinity_out=affinity)`` (bf16
         kind), given ``dout`` = dL/dy [T, d] bf16.  Fills ``dx``,
         ``drouter_w`` and, with ``weights``, ``dw13``, ``dw2``, ``dws13``,
         ``dws2`` (plus the intermediates ``dy_perm``, ``dgate``, ``dlogit``,
         ``dx_perm``, ``dx_shared``); returns ``dx``.  The selection and the
-        bias are those of the forward; the bias gets no gradient."""
+        bias are those of the forward; the bias gets no gradient.
+        ``events`` (four torch.cuda.Event) are recorded on ``stream`` around
+        the expert Dgrad call and around the expert Wgrad call."""
         c = self.cfg
         if c.dtype != "bf16":
             raise ValueError("the backward pass is implemented for the bf16 kind")
@@ -145,15 +147,23 @@ class MoELayer:
             moe_permute(c, x, self.token_of_row, self.x_perm, stream=stream)
         moe_combine_backward(c, dout, self.y_perm, self.row_of_slot, self.topk_w, self.dy_perm,
                              self.dgate, stream=stream)
+        if events is not None:
+            events[0].record(stream)
         moe_experts_backward_input(c, self.x_perm, x, self.offsets, self.w13, self.w2, self.ws13,
                                    self.ws2, self.dy_perm, dout, self.dx_perm, self.dx_shared,
                                    self.bws, stream=stream)
+        if events is not None:
+            events[1].record(stream)
         moe_route_backward(c, x, self.router_w, affinity, self.topk_idx, self.dgate,
                            self.row_of_slot, self.token_of_row, self.offsets, self.dx_perm,
                            self.dx_shared, self.dlogit, self.dx, self.drouter_w, self.bws,
                            stream=stream)
         if weights:
+            if events is not None:
+                events[2].record(stream)
             moe_experts_backward_weights(c, self.x_perm, x, self.offsets, self.dy_perm, dout,
                                          self.dw13, self.dw2, self.dws13, self.dws2, self.bws,
                                          stream=stream)
+            if events is not None:
+                events[3].record(stream)
         return self.dx
