@@ -82,7 +82,8 @@ def expert_bytes(shape, counts):
 def backward_flops(shape):
     """Algorithmic FLOPs of the expert backward: Dgrad (dh = dy W2 and
     dx = [da | db] W13) and Wgrad (dW2 and dW13), 6 d I per row each.  The
-    recomputation of [a | b] (4 d I per row) is not counted."""
+    recomputation of [a | b] (4 d I per row; only when the forward did not
+    keep it, i.e. with --dispatch gather) is not counted."""
     rows = shape.T * shape.k + shape.T * shape.n_shared
     return {"dgrad": 6.0 * shape.d * shape.inter * rows, "wgrad": 6.0 * shape.d * shape.inter * rows,
             "recompute": 4.0 * shape.d * shape.inter * rows}
@@ -90,9 +91,10 @@ def backward_flops(shape):
 
 def train_launches(shape, gather=False):
     """Kernels of one training step: the forward's, then combine backward,
-    the recompute, two Dgrad and two Wgrad GEMMs, the router backward's two
-    kernels, and a permute when the forward gathered its rows."""
-    return launches_per_step(shape, gather) + 1 + 1 + 2 + 2 + 2 + (1 if gather else 0)
+    two Dgrad and two Wgrad GEMMs, the router backward's two kernels, and,
+    when the forward gathered its rows, a permute and the recomputation of
+    the gate/up products."""
+    return launches_per_step(shape, gather) + 1 + 2 + 2 + 2 + (2 if gather else 0)
 
 
 def layer_flops(shape):
@@ -601,7 +603,8 @@ def run_train(args, shape, world, rank, local):
     stream = torch.cuda.current_stream()
 
     def step(xx, gg, ev=None):
-        layer.forward(xx, affinity_out=aff, expert_events=None if ev is None else ev[0:2])
+        layer.forward(xx, affinity_out=aff, expert_events=None if ev is None else ev[0:2],
+                      keep=not gather)
         return layer.backward(xx, gg, aff, events=None if ev is None else ev[2:6])
 
     for _ in range(args.warmup):
@@ -626,7 +629,7 @@ def run_train(args, shape, world, rank, local):
     clk = clocks.stop()
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     parts = {"forward experts": [e[0].elapsed_time(e[1]) for e in evs],
-             "backward experts, input (Dgrad + recompute)": [e[2].elapsed_time(e[3]) for e in evs],
+             "backward experts, input (Dgrad)": [e[2].elapsed_time(e[3]) for e in evs],
              "backward experts, weights (Wgrad)": [e[4].elapsed_time(e[5]) for e in evs]}
     if moe.moe_get_device_error() != 0:
         raise RuntimeError("device error in the timed region")
@@ -661,7 +664,7 @@ def run_train(args, shape, world, rank, local):
     peak_sust = peaks.get("bf16_tflops_sustained", peak)
     bf = backward_flops(shape)
     alg = {"forward experts": expert_flops(shape),
-           "backward experts, input (Dgrad + recompute)": bf["dgrad"],
+           "backward experts, input (Dgrad)": bf["dgrad"],
            "backward experts, weights (Wgrad)": bf["wgrad"]}
     breakdown = {}
     for k, v in parts.items():
@@ -680,8 +683,11 @@ def run_train(args, shape, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": describe(shape), "global_batch": world * shape.T,
-                   "step": "forward (route, permute, experts, combine, bias update) + backward "
-                           "(combine, experts Dgrad with [a|b] recomputed, router, experts Wgrad)",
+                   "step": "forward (route, permute, experts keeping [a|b], combine, bias update) + "
+                           "backward (combine, experts Dgrad, router, experts Wgrad)"
+                           if not gather else
+                           "forward (route, experts gathering rows, combine, bias update) + backward "
+                           "(permute, combine, experts Dgrad with [a|b] recomputed, router, experts Wgrad)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: every step streams all expert weights and "
                          "writes all weight gradients"},
@@ -691,7 +697,7 @@ def run_train(args, shape, world, rank, local):
                      "peak_kind": f"bf16 dense burst, {peaks['_source']}",
                      "frac_of_sustained": achieved / peak_sust, "traffic": None,
                      "breakdown": breakdown,
-                     "recompute_tflop_not_counted": bf["recompute"] / 1e12},
+                     "recompute_tflop_not_counted": bf["recompute"] / 1e12 if gather else 0.0},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": dx_host.numel() * dx_host.element_size(),

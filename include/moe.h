@@ -283,6 +283,8 @@ moe_status_t moe_balance_stat(const moe_cfg_t* cfg, const float* affinity,
  *     moe_combine_backward -> moe_experts_backward_input
  *         -> moe_route_backward        (dx and dL/de: input side complete)
  *         -> moe_experts_backward_weights
+ * (with moe_experts_grouped_train in place of moe_experts_grouped in the
+ * forward, the input call skips recomputing the gate/up products).
  * The weights call may run any time after the input call, on the same
  * workspace (it reads the intermediates the input call left there).
  *
@@ -319,9 +321,27 @@ moe_status_t moe_combine_backward(const moe_cfg_t* cfg, const void* dout, const 
                                   void* dy_perm, float* dgate, void* stream);
 
 /*
- * moe_experts_backward_input - Dgrad of every expert FFN: recomputes
- * [a | b] with the forward's grouped GEMM, then dh, the SwiGLU backward and
- * dx, leaving [da | db] and h in `ws` for moe_experts_backward_weights.
+ * moe_experts_grouped_train - moe_experts_grouped (BF16 kind) for a
+ * training step: the same outputs, and the gate/up epilogue also keeps
+ * a = x W1^T and b = x W3^T of every routed row and shared expert (bf16)
+ * in the backward workspace `bws`, so that moe_experts_backward_input with
+ * ab_kept = 1 does not recompute them (0.5 GB written at the DeepSeek-V3
+ * shape instead of 4.3 TFLOP recomputed).
+ *   arguments as in moe_experts_grouped (no scales), plus
+ *   bws, bws_bytes   at least moe_backward_workspace_bytes(cfg); pass the
+ *                    same buffer to the backward calls of this step
+ */
+moe_status_t moe_experts_grouped_train(const moe_cfg_t* cfg, const void* x_perm, const void* x,
+                                       const int32_t* offsets, const void* w13, const void* w2,
+                                       const void* ws13, const void* ws2, void* y_perm,
+                                       void* y_shared, void* ws, size_t ws_bytes, void* bws,
+                                       size_t bws_bytes, void* stream);
+
+/*
+ * moe_experts_backward_input - Dgrad of every expert FFN: [a | b] (kept by
+ * moe_experts_grouped_train, or recomputed with the forward's grouped
+ * GEMM), then dh, the SwiGLU backward and dx, leaving [da | db] (over
+ * [a | b]) and h in `ws` for moe_experts_backward_weights.
  *   x_perm [T*K, d], x [T, d]       bf16 forward inputs (routed / shared)
  *   offsets [E + 1]                 from moe_route
  *   w13, w2, ws13, ws2              as in moe_experts_grouped
@@ -330,14 +350,17 @@ moe_status_t moe_combine_backward(const moe_cfg_t* cfg, const void* dout, const 
  *   dx_perm [T*K, d]   bf16 out: routed experts' input gradient per row
  *   dx_shared [T, d]   bf16 out: sum of the shared experts' input
  *                      gradients (NULL if N_s = 0)
+ *   ab_kept            nonzero: `ws` holds [a | b] from this step's
+ *                      moe_experts_grouped_train (consumed: the call
+ *                      overwrites it with [da | db]); 0: recompute it
  *   ws, ws_bytes       at least moe_backward_workspace_bytes(cfg)
  */
 moe_status_t moe_experts_backward_input(const moe_cfg_t* cfg, const void* x_perm,
                                         const void* x, const int32_t* offsets, const void* w13,
                                         const void* w2, const void* ws13, const void* ws2,
                                         const void* dy_perm, const void* dout, void* dx_perm,
-                                        void* dx_shared, void* ws, size_t ws_bytes,
-                                        void* stream);
+                                        void* dx_shared, int32_t ab_kept, void* ws,
+                                        size_t ws_bytes, void* stream);
 
 /*
  * moe_experts_backward_weights - Wgrad of every expert FFN from the

@@ -41,7 +41,8 @@ EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_byt
             "moe_bias_update", "moe_quantize_weights_fp8", "moe_get_device_error",
             "moe_route_static_scratch", "moe_experts_grouped_gather", "moe_balance_stat",
             "moe_selftest_wait", "moe_backward_workspace_bytes", "moe_combine_backward",
-            "moe_experts_backward_input", "moe_experts_backward_weights", "moe_route_backward")
+            "moe_experts_backward_input", "moe_experts_backward_weights", "moe_route_backward",
+            "moe_experts_grouped_train")
 
 
 class MoeCfg(ctypes.Structure):
@@ -99,7 +100,10 @@ _lib.moe_route_static_scratch.argtypes = [_CFG] + [_P] * 11 + [_P]
 _lib.moe_backward_workspace_bytes.restype = ctypes.c_size_t
 _lib.moe_backward_workspace_bytes.argtypes = [_CFG]
 _lib.moe_combine_backward.argtypes = [_CFG] + [_P] * 6 + [_P]
-_lib.moe_experts_backward_input.argtypes = [_CFG] + [_P] * 11 + [_P, ctypes.c_size_t, _P]
+_lib.moe_experts_backward_input.argtypes = ([_CFG] + [_P] * 11 + [ctypes.c_int32] +
+                                            [_P, ctypes.c_size_t, _P])
+_lib.moe_experts_grouped_train.argtypes = ([_CFG] + [_P] * 10 + [ctypes.c_size_t] +
+                                           [_P, ctypes.c_size_t, _P])
 _lib.moe_experts_backward_weights.argtypes = [_CFG] + [_P] * 9 + [_P, ctypes.c_size_t, _P]
 _lib.moe_route_backward.argtypes = [_CFG] + [_P] * 13 + [_P, ctypes.c_size_t, _P]
 
@@ -305,16 +309,30 @@ def moe_combine_backward(cfg, dout, y_perm, row_of_slot, topk_w, dy_perm, dgate,
         _ptr(dy_perm, "dy_perm", _BF), _ptr(dgate, "dgate", torch.float32), _stream(stream)))
 
 
+def moe_experts_grouped_train(cfg, x_perm, x, offsets, w13, w2, ws13, ws2, y_perm, y_shared,
+                              ws, bws, stream=None):
+    """moe_experts_grouped (bf16) that also keeps [a | b] in the backward
+    workspace bws for moe_experts_backward_input(..., ab_kept=True)."""
+    _check("moe_experts_grouped_train", _lib.moe_experts_grouped_train(
+        _cfg(cfg), _ptr(x_perm, "x_perm", _BF), _ptr(x, "x", _BF, allow_none=True),
+        _ptr(offsets, "offsets", torch.int32), _ptr(w13, "w13", _BF), _ptr(w2, "w2", _BF),
+        _ptr(ws13, "ws13", _BF, allow_none=True), _ptr(ws2, "ws2", _BF, allow_none=True),
+        _ptr(y_perm, "y_perm", _BF), _ptr(y_shared, "y_shared", _BF, allow_none=True),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(),
+        _ptr(bws, "bws"), bws.numel() * bws.element_size(), _stream(stream)))
+
+
 def moe_experts_backward_input(cfg, x_perm, x, offsets, w13, w2, ws13, ws2, dy_perm, dout,
-                               dx_perm, dx_shared, ws, stream=None):
-    """Dgrad of the expert FFNs; leaves [da | db] and h in ws for the Wgrad."""
+                               dx_perm, dx_shared, ws, ab_kept=False, stream=None):
+    """Dgrad of the expert FFNs; leaves [da | db] and h in ws for the Wgrad.
+    ab_kept: ws holds [a | b] from this step's moe_experts_grouped_train."""
     _check("moe_experts_backward_input", _lib.moe_experts_backward_input(
         _cfg(cfg), _ptr(x_perm, "x_perm", _BF), _ptr(x, "x", _BF, allow_none=True),
         _ptr(offsets, "offsets", torch.int32), _ptr(w13, "w13", _BF), _ptr(w2, "w2", _BF),
         _ptr(ws13, "ws13", _BF, allow_none=True), _ptr(ws2, "ws2", _BF, allow_none=True),
         _ptr(dy_perm, "dy_perm", _BF), _ptr(dout, "dout", _BF, allow_none=True),
         _ptr(dx_perm, "dx_perm", _BF), _ptr(dx_shared, "dx_shared", _BF, allow_none=True),
-        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+        1 if ab_kept else 0, _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_experts_backward_weights(cfg, x_perm, x, offsets, dy_perm, dout, dw13, dw2, dws13, dws2,

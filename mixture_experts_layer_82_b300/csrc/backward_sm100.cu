@@ -548,7 +548,8 @@ cudaError_t launch_experts_bwd_input_bf16(const ExpertsBwdArgs& a, cudaStream_t 
   const ExpertsBwdScratch w = a.scratch;
 
   // ---- 1. recompute [a | b] = x W13^T with the forward's plain grouped GEMM
-  {
+  // (unless the training forward kept it)
+  if (!a.ab_kept) {
     using namespace bf16gemm;
     Params g{};
     g.offsets = a.offsets; g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;

@@ -55,6 +55,8 @@ struct ClassDesc {
   int ld_out;          // output row stride, elements
   int n_out;           // output columns (h columns for gate/up, d for down)
   int k_dim;           // reduction length
+  __nv_bfloat16* ab;   // gate/up, optional: [a | b] of every expert kept for the backward
+  int ld_ab;           // its row stride (2I per expert of the class)
 };
 
 struct Params {
@@ -368,6 +370,14 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
       const int n_base = tl.nt * out_tile_cols<MODE>();
       __nv_bfloat16* orow = cd.out + static_cast<size_t>(tl.row0 + (valid ? m : 0)) * cd.ld_out + n_base;
       if (MODE == GATEUP) {
+        // training forward: a and b of this row and these columns, kept for
+        // the backward at [expert of the columns][a | b] (a 128-column tile
+        // never straddles two shared experts: I % 128 == 0)
+        __nv_bfloat16* abrow =
+            cd.ab != nullptr && valid
+                ? cd.ab + static_cast<size_t>(tl.row0 + m) * cd.ld_ab +
+                      (n_base / p.inter) * 2 * p.inter + n_base % p.inter
+                : nullptr;
 #pragma unroll 1
         for (int c = 0; c < (BN / 2) / 16; ++c) {
           float a[16], b[16];
@@ -382,6 +392,18 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+          if (abrow != nullptr) {
+            uint4* da = reinterpret_cast<uint4*>(abrow + c * 16);
+            uint4* db = reinterpret_cast<uint4*>(abrow + p.inter + c * 16);
+            da[0] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                               pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+            da[1] = make_uint4(pack_bf16x2(a[8], a[9]), pack_bf16x2(a[10], a[11]),
+                               pack_bf16x2(a[12], a[13]), pack_bf16x2(a[14], a[15]));
+            db[0] = make_uint4(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]),
+                               pack_bf16x2(b[4], b[5]), pack_bf16x2(b[6], b[7]));
+            db[1] = make_uint4(pack_bf16x2(b[8], b[9]), pack_bf16x2(b[10], b[11]),
+                               pack_bf16x2(b[12], b[13]), pack_bf16x2(b[14], b[15]));
           }
         }
       } else {
@@ -493,8 +515,8 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
     g.b_map[1] = g.b_map[0];
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  g.cls[0] = ClassDesc{h_routed, I, I, c.d};
-  g.cls[1] = ClassDesc{h_shared, Ns * I, Ns * I, c.d};
+  g.cls[0] = ClassDesc{h_routed, I, I, c.d, a.ab, 2 * I};
+  g.cls[1] = ClassDesc{h_shared, Ns * I, Ns * I, c.d, a.ab_shared, Ns * 2 * I};
   cudaError_t e = gather ? launch_bf16_gemm<GATEUP, true>(g, st) : launch_bf16_gemm<GATEUP, false>(g, st);
   if (e != cudaSuccess) return e;
 

@@ -81,6 +81,8 @@ struct ExpertsArgs {
   const int32_t* token_of_row;  // non-null: gate/up gathers its routed A rows from x
   void* h;            // workspace: routed rows [T*K, I] then shared rows [T, Ns*I]
   float* h_scales;    // FP8: [T*K, I/128] then [T, Ns*I/128]
+  __nv_bfloat16* ab;         // bf16 training forward, optional: [a | b] rows kept for
+  __nv_bfloat16* ab_shared;  // the backward ([T*K, 2I] and [T, Ns*2I])
 };
 
 size_t experts_scratch_bytes(const moe_cfg_t& c);
@@ -115,6 +117,7 @@ struct ExpertsBwdArgs {
   void* dw2;
   void* dws13;
   void* dws2;
+  bool ab_kept;  // the forward kept [a | b] in the scratch: no recomputation
   ExpertsBwdScratch scratch;
 };
 

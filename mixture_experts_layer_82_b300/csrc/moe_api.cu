@@ -304,12 +304,42 @@ moe_status_t moe_combine_backward(const moe_cfg_t* cfg, const void* dout, const 
                                            dgate, as_stream(stream)));
 }
 
+moe_status_t moe_experts_grouped_train(const moe_cfg_t* cfg, const void* x_perm, const void* x,
+                                       const int32_t* offsets, const void* w13, const void* w2,
+                                       const void* ws13, const void* ws2, void* y_perm,
+                                       void* y_shared, void* ws, size_t ws_bytes, void* bws,
+                                       size_t bws_bytes, void* stream) {
+  moe_status_t st = check_backward_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (x_perm == nullptr || offsets == nullptr || w13 == nullptr || w2 == nullptr ||
+      y_perm == nullptr || ws == nullptr || bws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0 && (x == nullptr || ws13 == nullptr || ws2 == nullptr || y_shared == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_perm, x, offsets, w13, w2, ws13, ws2, y_perm, y_shared, ws, bws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  if (ws_bytes < experts_scratch_bytes(c) || bws_bytes < moe_backward_workspace_bytes(cfg))
+    return MOE_ERR_WORKSPACE;
+  ExpertsArgs a{};
+  a.cfg = &c;
+  a.x_perm = x_perm; a.x = x; a.offsets = offsets;
+  a.w13 = w13; a.w2 = w2; a.ws13 = ws13; a.ws2 = ws2;
+  a.y_perm = y_perm; a.y_shared = c.n_shared > 0 ? y_shared : nullptr;
+  experts_scratch_carve(c, ws, &a.h, &a.h_scales);
+  const ExpertsBwdScratch w = experts_bwd_scratch_carve(c, bws);
+  a.ab = w.ab;
+  a.ab_shared = w.ab_shared;
+  return from_cuda(launch_experts_bf16(a, as_stream(stream)));
+}
+
 moe_status_t moe_experts_backward_input(const moe_cfg_t* cfg, const void* x_perm,
                                         const void* x, const int32_t* offsets, const void* w13,
                                         const void* w2, const void* ws13, const void* ws2,
                                         const void* dy_perm, const void* dout, void* dx_perm,
-                                        void* dx_shared, void* ws, size_t ws_bytes,
-                                        void* stream) {
+                                        void* dx_shared, int32_t ab_kept, void* ws,
+                                        size_t ws_bytes, void* stream) {
   moe_status_t st = check_backward_cfg(cfg);
   if (st != MOE_OK) return st;
   const moe_cfg_t& c = *cfg;
@@ -330,6 +360,7 @@ moe_status_t moe_experts_backward_input(const moe_cfg_t* cfg, const void* x_perm
   a.w13 = w13; a.w2 = w2; a.ws13 = ws13; a.ws2 = ws2;
   a.dy_perm = dy_perm; a.dout = dout;
   a.dx_perm = dx_perm; a.dx_shared = c.n_shared > 0 ? dx_shared : nullptr;
+  a.ab_kept = ab_kept != 0;
   a.scratch = experts_bwd_scratch_carve(c, ws);
   return from_cuda(launch_experts_bwd_input_bf16(a, as_stream(stream)));
 }

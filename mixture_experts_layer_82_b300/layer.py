@@ -10,7 +10,7 @@ import torch
 from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_experts_grouped_gather,
                moe_combine, moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes,
                moe_backward_workspace_bytes, moe_combine_backward, moe_experts_backward_input,
-               moe_experts_backward_weights, moe_route_backward)
+               moe_experts_backward_weights, moe_route_backward, moe_experts_grouped_train)
 
 
 def _quantize(w, stream=None):
@@ -70,16 +70,22 @@ class MoELayer:
         self.ws = torch.empty(moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
 
     def forward(self, x, stream=None, update_bias=True, affinity_out=None, affinity_in=None,
-                expert_events=None, gather=None, out=None):
+                expert_events=None, gather=None, out=None, keep=False):
         """One forward step on ``x`` [T, d]; returns the layer output, written
         to ``out`` when given (else to the layer's own buffer).
         ``expert_events`` (a pair of torch.cuda.Event) are recorded on
         ``stream`` around the grouped expert GEMMs, for timing them inside a
         step.  ``gather`` (default: ``self.gather``) folds the permute into
-        the gate/up GEMM (moe_experts_grouped_gather; bf16 kind)."""
+        the gate/up GEMM (moe_experts_grouped_gather; bf16 kind).  ``keep``
+        (bf16 kind, permuting forward): keep the gate/up products for the
+        next ``backward`` instead of having it recompute them."""
         c = self.cfg
         out = self.out if out is None else out
         gather = self.gather if gather is None else gather
+        keep = keep and c.dtype == "bf16" and not gather
+        if keep and not hasattr(self, "bws"):
+            self._grad_buffers()
+        self._ab_kept = False
         moe_route(c, x, self.router_w, self.bias, self.topk_idx, self.topk_w, self.counts,
                   self.offsets, self.row_of_slot, self.token_of_row, self.ws,
                   affinity_in=affinity_in, affinity_out=affinity_out, stream=stream)
@@ -95,11 +101,17 @@ class MoELayer:
             shared_in = self.x_q if c.dtype == "fp8" else x
             if expert_events is not None:
                 expert_events[0].record(stream)
-            moe_experts_grouped(c, self.x_perm, shared_in, self.offsets, self.w13, self.w2,
-                                self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
-                                x_perm_scales=self.x_perm_s, x_scales=self.x_q_s,
-                                w13_scales=self.w13_s, w2_scales=self.w2_s,
-                                ws13_scales=self.ws13_s, ws2_scales=self.ws2_s, stream=stream)
+            if keep:
+                moe_experts_grouped_train(c, self.x_perm, x, self.offsets, self.w13, self.w2,
+                                          self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
+                                          self.bws, stream=stream)
+                self._ab_kept = True
+            else:
+                moe_experts_grouped(c, self.x_perm, shared_in, self.offsets, self.w13, self.w2,
+                                    self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
+                                    x_perm_scales=self.x_perm_s, x_scales=self.x_q_s,
+                                    w13_scales=self.w13_s, w2_scales=self.w2_s,
+                                    ws13_scales=self.ws13_s, ws2_scales=self.ws2_s, stream=stream)
         if expert_events is not None:
             expert_events[1].record(stream)
         moe_combine(c, self.y_perm, self.y_shared, self.row_of_slot, self.topk_w, out,
@@ -130,7 +142,8 @@ class MoELayer:
 
     def backward(self, x, dout, affinity, stream=None, weights=True, events=None):
         """Backward of the last ``forward(x, affinity_out=affinity)`` (bf16
-        kind), given ``dout`` = dL/dy [T, d] bf16.  Fills ``dx``,
+        kind; with ``keep=True`` there, the gate/up products are not
+        recomputed), given ``dout`` = dL/dy [T, d] bf16.  Fills ``dx``,
         ``drouter_w`` and, with ``weights``, ``dw13``, ``dw2``, ``dws13``,
         ``dws2`` (plus the intermediates ``dy_perm``, ``dgate``, ``dlogit``,
         ``dx_perm``, ``dx_shared``); returns ``dx``.  The selection and the
@@ -151,7 +164,9 @@ class MoELayer:
             events[0].record(stream)
         moe_experts_backward_input(c, self.x_perm, x, self.offsets, self.w13, self.w2, self.ws13,
                                    self.ws2, self.dy_perm, dout, self.dx_perm, self.dx_shared,
-                                   self.bws, stream=stream)
+                                   self.bws, ab_kept=getattr(self, "_ab_kept", False),
+                                   stream=stream)
+        self._ab_kept = False  # consumed: [da | db] now lies over it
         if events is not None:
             events[1].record(stream)
         moe_route_backward(c, x, self.router_w, affinity, self.topk_idx, self.dgate,

@@ -35,9 +35,11 @@ def _layer(shape):
     return L, layer
 
 
-def _run(shape, L, layer):
+def _run(shape, L, layer, keep=True):
+    """Training forward (keeping the gate/up products unless ``keep`` is
+    False) and backward."""
     aff = torch.empty(shape.T, shape.E, dtype=torch.float32, device=DEV)
-    layer.forward(L["x"], affinity_out=aff, update_bias=False)
+    layer.forward(L["x"], affinity_out=aff, update_bias=False, keep=keep)
     dout = make_grad(shape, DEV)
     layer.backward(L["x"], dout, aff)
     assert moe.moe_get_device_error() == 0
@@ -97,17 +99,33 @@ def test_backward_is_deterministic():
     aff, dout = _run(shape, L, layer)
     names = ("dx", "drouter_w", "dw13", "dw2", "dws13", "dws2", "dgate", "dlogit")
     first = {k: getattr(layer, k).clone() for k in names}
-    layer.backward(L["x"], dout, aff)
-    assert moe.moe_get_device_error() == 0
+    _run(shape, L, layer)
     for k, v in first.items():
         bits = torch.int16 if v.dtype == torch.bfloat16 else torch.int32
         assert torch.equal(getattr(layer, k).view(bits), v.view(bits)), k
 
 
+def test_kept_gate_up_products_match_recomputed():
+    """moe_experts_grouped_train keeps [a | b] from the forward's gate/up
+    epilogue; the backward that uses them matches the one that recomputes
+    them, and the training forward's own outputs equal the plain forward's
+    bit for bit."""
+    shape = SHAPES[1]
+    L, layer = _layer(shape)
+    _run(shape, L, layer, keep=False)
+    ref = {k: getattr(layer, k).clone() for k in
+           ("y_perm", "y_shared", "dx", "drouter_w", "dw13", "dw2", "dws13", "dws2")}
+    _run(shape, L, layer, keep=True)
+    for k in ("y_perm", "y_shared"):
+        assert torch.equal(getattr(layer, k), ref[k]), k
+    for k in ("dx", "drouter_w", "dw13", "dw2", "dws13", "dws2"):
+        assert rel_frobenius(host(getattr(layer, k)), host(ref[k])) < 1e-3, k
+
+
 def test_gathering_forward_gives_the_same_backward():
     shape = SHAPES[1]
     L, layer = _layer(shape)
-    aff, dout = _run(shape, L, layer)
+    aff, dout = _run(shape, L, layer, keep=False)
     ref = {k: getattr(layer, k).clone() for k in ("dx", "drouter_w", "dw13", "dw2")}
     layer.gather = True
     aff2 = torch.empty_like(aff)
