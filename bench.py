@@ -380,7 +380,8 @@ def run_reference(args, shape, world, rank):
         return 0
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     L = make_layer(shape, dev)
-    fn = oracle_train_sample if args.train else oracle_sample
+    train = getattr(args, "train", False)
+    fn = oracle_train_sample if train else oracle_sample
     for i in range(args.warmup):
         fn(shape, L, args.ref_tokens, token0=i * args.ref_tokens)
     secs, toks = 0.0, 0
@@ -393,9 +394,9 @@ def run_reference(args, shape, world, rank):
     cores = blas_threads()
     sample = (f"{args.ref_tokens} tokens of the {shape.name} batch per step, end to end "
               f"(affinity, group-limited top-k, gates, shared + routed SwiGLU experts in fp64, "
-              f"combine{'; then the whole backward' if args.train else ''}); expert weights "
+              f"combine{'; then the whole backward' if train else ''}); expert weights "
               f"fetched from device memory per expert")
-    line = {"impl": "reference", "metric": METRIC_TRAIN if args.train else METRIC,
+    line = {"impl": "reference", "metric": METRIC_TRAIN if train else METRIC,
             "value": value, "unit": "tokens/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,

@@ -140,3 +140,54 @@ def test_binding_refuses_host_tensors():
     with pytest.raises(ValueError):
         moe.moe_bias_update(_base(), torch.zeros(64, dtype=torch.int32),
                             torch.zeros(64, dtype=torch.float32), stream=0)
+
+
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+def test_backward_workspace_formula_and_kinds():
+    c = _base()  # mid-size bf16 layer: T=4096, K=6, N_s=2, I=1408
+    tk, T, I, ns = c.T * c.k, c.T, c.inter, c.n_shared
+    assert moe.moe_backward_workspace_bytes(c) == (_align256((tk + T * ns) * 3 * I * 2)
+                                                   + _align256(tk * 4))
+    # the backward exists for the bf16 kind only, and for at most 64 shared experts
+    assert moe.moe_backward_workspace_bytes(_base(dtype="fp32")) == 0
+    assert moe.moe_backward_workspace_bytes(_base(dtype="fp8")) == 0
+    assert moe.moe_backward_workspace_bytes(_base(n_shared=65)) == 0
+    assert moe.moe_backward_workspace_bytes(_base(d=2000)) == 0
+
+
+def test_backward_calls_check_before_launching():
+    lib = moe.library()
+    bf = ctypes.byref(_base().c())
+    fp32 = ctypes.byref(_base(dtype="fp32").c())
+    a = 0x100000
+    ws = moe.moe_backward_workspace_bytes(_base())
+    # combine backward: kind, null, alignment
+    assert lib.moe_combine_backward(fp32, a, a, a, a, a, a, None) == 2
+    assert lib.moe_combine_backward(bf, a, None, a, a, a, a, None) == 1
+    assert lib.moe_combine_backward(bf, a, a, a, a, a + 4, a, None) == 3
+    # input call: missing shared-expert pointers, small workspace, misaligned
+    p = [a] * 11
+    q = list(p); q[5] = None  # ws13 with N_s = 2
+    assert lib.moe_experts_backward_input(bf, *q, 0, a, ws, None) == 1
+    assert lib.moe_experts_backward_input(bf, *p, 0, a, ws - 1, None) == 7
+    q = list(p); q[9] = a + 8  # dx_perm misaligned
+    assert lib.moe_experts_backward_input(bf, *q, 0, a, ws, None) == 3
+    # weights call
+    p = [a] * 9
+    assert lib.moe_experts_backward_weights(fp32, *p, a, ws, None) == 2
+    q = list(p); q[5] = None  # dw13
+    assert lib.moe_experts_backward_weights(bf, *q, a, ws, None) == 1
+    assert lib.moe_experts_backward_weights(bf, *p, a, 16, None) == 7
+    # route backward
+    p = [a] * 13
+    q = list(p); q[2] = None  # affinity
+    assert lib.moe_route_backward(bf, *q, a, ws, None) == 1
+    assert lib.moe_route_backward(bf, *p, a, 16, None) == 7
+    # training forward: the backward workspace must be large enough
+    p = [a] * 10
+    big = moe.moe_workspace_bytes(_base())
+    assert lib.moe_experts_grouped_train(bf, *p, big, a, ws - 1, None) == 7
+    assert lib.moe_experts_grouped_train(fp32, *p, big, a, ws, None) == 2
