@@ -9,8 +9,10 @@ input already resident in device memory.  The default workload is the
 DeepSeek-V3-shaped layer in bf16 (T=8192, d=7168, 256 routed experts in 8
 groups, top-4 groups, top-8, 1 shared expert, I=2048, route scale 2.5, Zipf
 -skewed router).  With N > 1 (torchrun) every rank runs its own replica on
-its own batch (weak scaling, no collective on the data path); the time is
-the maximum over ranks.  Rank 0 prints one JSON line.
+its own batch (weak scaling, no collective on the data path; the replicas
+sum their per-expert loads with one all-reduce of counts[E] per step so that
+the bias update sees the whole batch); the time is the maximum over ranks.
+Rank 0 prints one JSON line.
 
 ``--train`` (bf16 kind) makes a step one training pass instead: the forward
 above, then its backward (combine backward, expert Dgrad with the gate/up
@@ -423,8 +425,13 @@ def run_ours(args, shape, world, rank, local):
                          gather=gather)
     x = L["x"]
     stream = torch.cuda.current_stream()
+    # data-parallel replicas sum their per-expert loads for the bias update
+    lg = None
+    if world > 1:
+        import torch.distributed as dist
+        lg = dist.group.WORLD
     for _ in range(args.warmup):
-        layer.forward(x)
+        layer.forward(x, load_group=lg)
     torch.cuda.synchronize()
     status = moe.moe_get_device_error()
     if status != 0:
@@ -441,7 +448,7 @@ def run_ours(args, shape, world, rank, local):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(K):
-        layer.forward(x, expert_events=ev_exp[i])
+        layer.forward(x, expert_events=ev_exp[i], load_group=lg)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -493,7 +500,7 @@ def run_ours(args, shape, world, rank, local):
             stream.wait_event(h2d_done[b])
             if used[b]:
                 stream.wait_event(d2h_done[b])  # step i-2's output has been read back
-            layer.forward(x_dev[b], out=out_dev[b])
+            layer.forward(x_dev[b], out=out_dev[b], load_group=lg)
             comp_done[b].record(stream)
             used[b] = True
             d2h_s.wait_event(comp_done[b])
@@ -530,7 +537,8 @@ def run_ours(args, shape, world, rank, local):
         peak = peaks["bf16_tflops"]
         peak_sust = peaks.get("bf16_tflops_sustained", peak)
         peak_kind = f"bf16 dense burst, {peaks['_source']}"
-    ebytes, touched = expert_bytes(shape, layer.counts.cpu().numpy())
+    # this replica's loads (counts hold the summed loads when replicas > 1)
+    ebytes, touched = expert_bytes(shape, np.diff(layer.offsets.cpu().numpy()))
     hbm_achieved = ebytes / (exp_mean * 1e-3) / 1e9
     kernel = (f"experts_{shape.dtype}_kernel (gate/up + down launches of one "
               f"moe_experts_grouped call)")
@@ -557,7 +565,8 @@ def run_ours(args, shape, world, rank, local):
         "config": {"workload": describe(shape), "global_batch": world * shape.T,
                    "dispatch": "gather rows inside the gate/up GEMM" if gather
                                else "permute kernel before the expert GEMMs",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "parallelism": f"data-parallel replicas x{world}, one all-reduce of the "
+                                  f"per-expert loads per step" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: every step streams all expert weights "
                          f"({(3 * shape.d * shape.inter * (shape.E + shape.n_shared)) * (1 if shape.dtype == 'fp8' else 2) / 1e9:.1f} GB)"},
         "layer_tflops": layer_flops(shape) * world * K / (total_ms * 1e-3) / 1e12,
@@ -603,9 +612,14 @@ def run_train(args, shape, world, rank, local):
     aff = torch.empty(shape.T, shape.E, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    lg = None
+    if world > 1:
+        import torch.distributed as dist
+        lg = dist.group.WORLD
+
     def step(xx, gg, ev=None):
         layer.forward(xx, affinity_out=aff, expert_events=None if ev is None else ev[0:2],
-                      keep=not gather)
+                      keep=not gather, load_group=lg)
         return layer.backward(xx, gg, aff, events=None if ev is None else ev[2:6])
 
     for _ in range(args.warmup):
@@ -689,7 +703,8 @@ def run_train(args, shape, world, rank, local):
                            if not gather else
                            "forward (route, experts gathering rows, combine, bias update) + backward "
                            "(permute, combine, experts Dgrad with [a|b] recomputed, router, experts Wgrad)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "parallelism": f"data-parallel replicas x{world}, one all-reduce of the "
+                                  f"per-expert loads per step" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: every step streams all expert weights and "
                          "writes all weight gradients"},
         "layer_tflops": step_flops * world * K / (total_ms * 1e-3) / 1e12,

@@ -7,6 +7,7 @@ from __future__ import annotations
 
 import torch
 
+from .replicas import global_cfg, global_load
 from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_experts_grouped_gather,
                moe_combine, moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes,
                moe_backward_workspace_bytes, moe_combine_backward, moe_experts_backward_input,
@@ -70,7 +71,7 @@ class MoELayer:
         self.ws = torch.empty(moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
 
     def forward(self, x, stream=None, update_bias=True, affinity_out=None, affinity_in=None,
-                expert_events=None, gather=None, out=None, keep=False):
+                expert_events=None, gather=None, out=None, keep=False, load_group=None):
         """One forward step on ``x`` [T, d]; returns the layer output, written
         to ``out`` when given (else to the layer's own buffer).
         ``expert_events`` (a pair of torch.cuda.Event) are recorded on
@@ -78,7 +79,10 @@ class MoELayer:
         step.  ``gather`` (default: ``self.gather``) folds the permute into
         the gate/up GEMM (moe_experts_grouped_gather; bf16 kind).  ``keep``
         (bf16 kind, permuting forward): keep the gate/up products for the
-        next ``backward`` instead of having it recompute them."""
+        next ``backward`` instead of having it recompute them.
+        ``load_group``: a torch.distributed group of data-parallel replicas;
+        the bias update then uses the whole batch's per-expert loads (one
+        all-reduce of ``counts``, which afterwards hold the global loads)."""
         c = self.cfg
         out = self.out if out is None else out
         gather = self.gather if gather is None else gather
@@ -117,7 +121,11 @@ class MoELayer:
         moe_combine(c, self.y_perm, self.y_shared, self.row_of_slot, self.topk_w, out,
                     stream=stream)
         if update_bias:
-            moe_bias_update(c, self.counts, self.bias, stream=stream)
+            if load_group is not None:
+                world = global_load(self.counts, load_group)
+                moe_bias_update(global_cfg(c, world), self.counts, self.bias, stream=stream)
+            else:
+                moe_bias_update(c, self.counts, self.bias, stream=stream)
         return out
 
     # ------------------------------------------------------------- backward
