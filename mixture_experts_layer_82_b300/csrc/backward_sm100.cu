@@ -18,8 +18,9 @@
 //
 // One persistent kernel per GEMM, three kinds:
 //   DG_SWIGLU  dh tile = dy rows x W2 (A K-major, B MN-major); the epilogue
-//              reads the recomputed [a | b] rows, writes [da | db] over them
-//              and h = silu(a) b (kept for dW2)
+//              reads the [a | b] rows (kept by the training forward, or
+//              recomputed), writes [da | db] over them and h = silu(a) b
+//              (kept for dW2)
 //   DG_PLAIN   dx tile = [da | db] rows x W13 (A K-major, B MN-major)
 //   WG         dW tile = A^T B over the rows of one segment (both
 //              MN-major); K is the segment length, so the last K block is
@@ -442,7 +443,8 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
           tmem_ld_wait();
           if (!valid || n_base + c * 16 >= p.n_dim) continue;
           if (KIND == DG_SWIGLU) {
-            // v = dh; [a | b] of the same row and columns, recomputed
+            // v = dh; [a | b] of the same row and columns (kept by the
+            // training forward, or recomputed)
             __nv_bfloat16* arow = cd.ab + row * cd.ld_ab + tl.j * cd.ab_col_step + n_base + c * 16;
             __nv_bfloat16* brow = arow + p.n_dim;
             uint4 araw[2], braw[2];
