@@ -53,3 +53,10 @@ from .moe_backward import (  # noqa: F401
     router_weight_grad,
     moe_layer_backward,
 )
+from .moe_fp8_backward import (  # noqa: F401
+    quantize_act_128x1,
+    dequantize_act_128x1,
+    fp8_dgrad,
+    fp8_wgrad,
+    fp8_swiglu_ffn_backward,
+)
