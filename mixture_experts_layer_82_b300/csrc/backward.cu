@@ -148,12 +148,14 @@ __global__ void __launch_bounds__(kWarps * 32) route_backward_kernel(
 __global__ void __launch_bounds__(kWarps * 32) router_wgrad_kernel(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ token_of_row,
     const int32_t* __restrict__ offsets, const float* __restrict__ dlogit_row,
-    float* __restrict__ drouter_w, int T, int d) {
+    float* __restrict__ drouter_w, int T, int n_rows, int d) {
   __shared__ float part[kWarps][256];
   const int e = blockIdx.x;
   const int c0 = blockIdx.y * 256;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int r0 = offsets[e], r1 = offsets[e + 1];
+  int r0;
+  const int nr = checked_segment(offsets, e, n_rows, r0);
+  const int r1 = r0 + nr;
   const int c = c0 + lane * 8;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (c < d) {
@@ -211,7 +213,8 @@ cudaError_t launch_route_backward(const moe_cfg_t& c, const RouteBwdArgs& a, cud
   const dim3 grid(c.E, (c.d + 255) / 256);
   router_wgrad_kernel<<<grid, kWarps * 32, 0, st>>>(static_cast<const __nv_bfloat16*>(a.x),
                                                      a.token_of_row, a.offsets, a.dlogit_row,
-                                                     a.drouter_w, c.T, c.d);
+                                                     a.drouter_w, c.T,
+                                                     static_cast<int>(static_cast<int64_t>(c.T) * c.K), c.d);
   return cudaGetLastError();
 }
 

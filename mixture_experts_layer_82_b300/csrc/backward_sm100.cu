@@ -77,6 +77,7 @@ struct Params {
   CUtensorMap b_map[2];
   ClassDesc cls[2];
   const int32_t* offsets;
+  int n_rows;  // T * K: permuted rows, the bound of every segment
   int E;
   int T;
   int n_sh;   // groups of the shared class
@@ -129,8 +130,8 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
   for (int g = g0; g < g1; ++g) {
     int rows;
     if (g < p.E) {
-      const int o0 = p.offsets[g];
-      rows = p.offsets[g + 1] - o0;
+      int o0;
+      rows = checked_segment(p.offsets, g, p.n_rows, o0);
       s.off[g] = o0;
     } else {
       rows = p.T;
@@ -504,14 +505,9 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
 template <int KIND>
 static cudaError_t launch_bwd_gemm(const bwdgemm::Params& prm, cudaStream_t st) {
   using namespace bwdgemm;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_gemm_kernel<KIND>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(bwd_gemm_kernel<KIND>),
+                                    static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
   bwd_gemm_kernel<KIND><<<sm_count(), THREADS, kSmemBytes, st>>>(prm);
   return cudaGetLastError();
 }
@@ -554,7 +550,7 @@ cudaError_t launch_experts_bwd_input_bf16(const ExpertsBwdArgs& a, cudaStream_t 
   if (!a.ab_kept) {
     using namespace bf16gemm;
     Params g{};
-    g.offsets = a.offsets; g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
+    g.offsets = a.offsets; g.n_rows = static_cast<int>(tk); g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
     g.d = 2 * I;   // B rows of one routed matrix
     g.inter = d;   // K of one matrix
     CUresult r = encode_bf16_2d(&g.a_map[0], a.x_perm, d, tk, BK, BM);
@@ -578,7 +574,7 @@ cudaError_t launch_experts_bwd_input_bf16(const ExpertsBwdArgs& a, cudaStream_t 
   using namespace bwdgemm;
   // ---- 2. dh = dy W2; [da | db] over [a | b]; h
   Params p{};
-  p.offsets = a.offsets; p.E = c.E; p.T = c.T;
+  p.offsets = a.offsets; p.n_rows = static_cast<int>(static_cast<int64_t>(c.T) * c.K); p.E = c.E; p.T = c.T;
   p.n_sh = Ns;
   p.n_dim = I;
   CUresult r = encode_bf16_2d(&p.a_map[0], a.dy_perm, d, tk, BK, BM);
@@ -600,7 +596,7 @@ cudaError_t launch_experts_bwd_input_bf16(const ExpertsBwdArgs& a, cudaStream_t 
 
   // ---- 3. dx = [da | db] W13 (routed rows; the shared experts' sum in one group)
   Params q{};
-  q.offsets = a.offsets; q.E = c.E; q.T = c.T;
+  q.offsets = a.offsets; q.n_rows = static_cast<int>(static_cast<int64_t>(c.T) * c.K); q.E = c.E; q.T = c.T;
   q.n_sh = has_shared ? 1 : 0;
   q.n_dim = d;
   r = encode_bf16_2d(&q.a_map[0], w.ab, 2 * I, tk, BK, BM);
@@ -632,7 +628,7 @@ cudaError_t launch_experts_bwd_weights_bf16(const ExpertsBwdArgs& a, cudaStream_
 
   // ---- dW2 = dy^T h: M = d, N = I, K = the rows of the segment
   Params p{};
-  p.offsets = a.offsets; p.E = c.E; p.T = c.T;
+  p.offsets = a.offsets; p.n_rows = static_cast<int>(static_cast<int64_t>(c.T) * c.K); p.E = c.E; p.T = c.T;
   p.n_sh = Ns;
   p.m_dim = d;
   p.n_dim = I;
@@ -655,7 +651,7 @@ cudaError_t launch_experts_bwd_weights_bf16(const ExpertsBwdArgs& a, cudaStream_
 
   // ---- dW13 = [da | db]^T x: M = 2I, N = d
   Params q{};
-  q.offsets = a.offsets; q.E = c.E; q.T = c.T;
+  q.offsets = a.offsets; q.n_rows = static_cast<int>(static_cast<int64_t>(c.T) * c.K); q.E = c.E; q.T = c.T;
   q.n_sh = Ns;
   q.m_dim = 2 * I;
   q.n_dim = d;

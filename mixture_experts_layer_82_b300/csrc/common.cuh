@@ -7,6 +7,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "moe.h"
 
 namespace moe {
@@ -23,6 +27,23 @@ enum : uint32_t {
 __device__ uint32_t g_error_word = 0;
 
 __device__ __forceinline__ void raise_error(uint32_t bits) { atomicOr(&g_error_word, bits); }
+
+// Rows of the segment [offsets[g], offsets[g + 1]) of routed group g, read
+// from device memory; `start` receives offsets[g] as read.  A segment that
+// runs backwards or leaves [0, n_rows] is an index error: it sets the error
+// word and counts as empty (0 rows), so no kernel reads or writes a
+// permuted row outside its buffers.  (The rows of a valid group are always
+// offsets[g + 1] - offsets[g], whatever its neighbours hold.)
+__device__ __forceinline__ int checked_segment(const int32_t* offsets, int g, int64_t n_rows,
+                                               int& start) {
+  const int o0 = offsets[g], o1 = offsets[g + 1];
+  start = o0;
+  if (o0 < 0 || o1 < o0 || static_cast<int64_t>(o1) > n_rows) {
+    raise_error(kErrIndex);
+    return 0;
+  }
+  return o1 - o0;
+}
 
 // ------------------------------------------------------------------ helpers
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -360,5 +381,41 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
+
+// ------------------------------------------------------ per-device set-up
+// Host-side state that depends on the device is kept per device ordinal, so
+// that one process may drive several GPUs (each call runs on the device that
+// is current on the calling thread).
+
+// Number of SMs of the current device, queried once per device.
+inline int sm_count() {
+  static std::mutex mu;
+  static int n[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  if (n[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    n[dev] = v;
+  }
+  return n[dev];
+}
+
+// Raises the dynamic shared-memory limit of kernel `func` to `bytes` on the
+// current device, once per (device, kernel).
+inline cudaError_t ensure_smem_limit(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({dev, func})) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({dev, func});
+  return e;
+}
 
 }  // namespace moe

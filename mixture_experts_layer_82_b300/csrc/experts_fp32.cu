@@ -25,14 +25,15 @@ struct SimtGroup {
 
 // Maps a linear M-tile index to its group: routed experts first (offsets
 // from device memory), then the shared class.  Returns false past the end.
-__device__ bool simt_find_group(const int32_t* offsets, int E, int T, bool has_shared, int lin,
-                                SimtGroup& g) {
+__device__ bool simt_find_group(const int32_t* offsets, int E, int T, int n_rows, bool has_shared,
+                                int lin, SimtGroup& g) {
   int acc = 0;
   for (int e = 0; e < E; ++e) {
-    const int rows = offsets[e + 1] - offsets[e];
+    int row0;
+    const int rows = checked_segment(offsets, e, n_rows, row0);
     const int nt = ceil_div(rows, kSBM);
     if (lin < acc + nt) {
-      g = SimtGroup{0, e, offsets[e], rows, lin - acc};
+      g = SimtGroup{0, e, row0, rows, lin - acc};
       return true;
     }
     acc += nt;
@@ -48,9 +49,9 @@ __device__ bool simt_find_group(const int32_t* offsets, int E, int T, bool has_s
 __global__ void __launch_bounds__(256) simt_gateup_kernel(
     const float* __restrict__ x_perm, const float* __restrict__ x, const int32_t* __restrict__ offsets,
     const float* __restrict__ w13, const float* __restrict__ ws13, float* __restrict__ h_routed,
-    float* __restrict__ h_shared, int E, int T, int d, int inter, int n_shared) {
+    float* __restrict__ h_shared, int E, int T, int n_rows, int d, int inter, int n_shared) {
   SimtGroup g;
-  if (!simt_find_group(offsets, E, T, n_shared > 0, blockIdx.y, g)) return;
+  if (!simt_find_group(offsets, E, T, n_rows, n_shared > 0, blockIdx.y, g)) return;
   const int ncols = g.cls == 0 ? inter : n_shared * inter;
   const int n0 = blockIdx.x * kSBN;
   if (n0 >= ncols) return;
@@ -111,10 +112,10 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(
 __global__ void __launch_bounds__(256) simt_down_kernel(
     const float* __restrict__ h_routed, const float* __restrict__ h_shared,
     const int32_t* __restrict__ offsets, const float* __restrict__ w2, const float* __restrict__ ws2,
-    float* __restrict__ y_perm, float* __restrict__ y_shared, int E, int T, int d, int inter,
+    float* __restrict__ y_perm, float* __restrict__ y_shared, int E, int T, int n_rows, int d, int inter,
     int n_shared) {
   SimtGroup g;
-  if (!simt_find_group(offsets, E, T, n_shared > 0, blockIdx.y, g)) return;
+  if (!simt_find_group(offsets, E, T, n_rows, n_shared > 0, blockIdx.y, g)) return;
   const int kdim = g.cls == 0 ? inter : n_shared * inter;
   const int n0 = blockIdx.x * kSBN;
   if (n0 >= d) return;
@@ -177,13 +178,13 @@ cudaError_t launch_experts_fp32(const ExpertsArgs& a, cudaStream_t st) {
   simt_gateup_kernel<<<dim3(ceil_div(n_gate, kSBN), m_tiles), 256, 0, st>>>(
       static_cast<const float*>(a.x_perm), static_cast<const float*>(a.x), a.offsets,
       static_cast<const float*>(a.w13), static_cast<const float*>(a.ws13), h_routed, h_shared, c.E,
-      c.T, c.d, c.inter, c.n_shared);
+      c.T, static_cast<int>(tk), c.d, c.inter, c.n_shared);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   simt_down_kernel<<<dim3(ceil_div(c.d, kSBN), m_tiles), 256, 0, st>>>(
       h_routed, h_shared, a.offsets, static_cast<const float*>(a.w2),
       static_cast<const float*>(a.ws2), static_cast<float*>(a.y_perm),
-      static_cast<float*>(a.y_shared), c.E, c.T, c.d, c.inter, c.n_shared);
+      static_cast<float*>(a.y_shared), c.E, c.T, static_cast<int>(tk), c.d, c.inter, c.n_shared);
   return cudaGetLastError();
 }
 

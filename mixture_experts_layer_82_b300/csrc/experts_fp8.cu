@@ -87,6 +87,7 @@ struct Params {
   CUtensorMap b_map[2];  // [0] routed weights, [1] shared weights
   ClassDesc cls[2];
   const int32_t* offsets;
+  int n_rows;  // T * K: permuted rows, the bound of every segment
   int E;
   int T;
   int has_shared;
@@ -141,8 +142,8 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
   for (int g = g0; g < g1; ++g) {
     int rows, cls;
     if (g < p.E) {
-      const int o0 = p.offsets[g];
-      rows = p.offsets[g + 1] - o0;
+      int o0;
+      rows = checked_segment(p.offsets, g, p.n_rows, o0);
       cls = 0;
       s.off[g] = o0;
     } else {
@@ -585,14 +586,9 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
 template <int MODE>
 static cudaError_t launch_fp8_gemm(const fp8gemm::Params& prm, cudaStream_t st) {
   using namespace fp8gemm;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(experts_fp8_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(experts_fp8_kernel<MODE>),
+                                    static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
   experts_fp8_kernel<MODE><<<sm_count(), THREADS, kSmemBytes, st>>>(prm);
   return cudaGetLastError();
 }
@@ -612,7 +608,7 @@ cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t st) {
 
   // ---- gate/up: A = x_perm / x_q (E4M3), B = W13 (E4M3)
   Params g{};
-  g.offsets = a.offsets; g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
+  g.offsets = a.offsets; g.n_rows = static_cast<int>(tk); g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
   g.inter = I; g.d = c.d;
   CUresult r = encode_tensor_map_2d(&g.a_map[0], U8, const_cast<void*>(a.x_perm), c.d, tk,
                                     static_cast<uint64_t>(c.d), BK, BM, SW);

@@ -64,6 +64,7 @@ struct Params {
   CUtensorMap b_map[2];  // [0] routed weights, [1] shared weights
   ClassDesc cls[2];
   const int32_t* offsets;
+  int n_rows;  // T * K: permuted rows, the bound of every segment
   int E;
   int T;
   int has_shared;
@@ -120,8 +121,8 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
   for (int g = g0; g < g1; ++g) {
     int rows, cls;
     if (g < p.E) {
-      const int o0 = p.offsets[g];
-      rows = p.offsets[g + 1] - o0;
+      int o0;
+      rows = checked_segment(p.offsets, g, p.n_rows, o0);
       cls = 0;
       s.off[g] = o0;
     } else {
@@ -437,17 +438,6 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
 }  // namespace bf16gemm
 
 // ------------------------------------------------------------------- host
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 size_t experts_scratch_bytes(const moe_cfg_t& c) {
   const size_t tk = static_cast<size_t>(c.T) * c.K;
   const size_t hr = tk * c.inter, hs = static_cast<size_t>(c.T) * c.n_shared * c.inter;
@@ -469,14 +459,9 @@ void experts_scratch_carve(const moe_cfg_t& c, void* ws, void** h, float** h_sca
 template <int MODE, bool GATHER>
 static cudaError_t launch_bf16_gemm(const bf16gemm::Params& prm, cudaStream_t st) {
   using namespace bf16gemm;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(experts_bf16_kernel<MODE, GATHER>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(experts_bf16_kernel<MODE, GATHER>),
+                                    static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
   experts_bf16_kernel<MODE, GATHER>
       <<<sm_count(), GATHER ? THREADS_GATHER : THREADS, kSmemBytes, st>>>(prm);
   return cudaGetLastError();
@@ -496,7 +481,7 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
   // ---- gate/up: A = x_perm (or, gathering, x[token_of_row]) / x, B = W13
   const bool gather = a.token_of_row != nullptr;
   Params g{};
-  g.offsets = a.offsets; g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
+  g.offsets = a.offsets; g.n_rows = static_cast<int>(tk); g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
   g.inter = I; g.d = c.d;
   g.token_of_row = a.token_of_row;
   g.x_rows = static_cast<const __nv_bfloat16*>(a.x);

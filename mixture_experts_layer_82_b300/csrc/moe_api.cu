@@ -241,8 +241,12 @@ moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y_perm, const void* y
 
 moe_status_t moe_bias_update(const moe_cfg_t* cfg, const int32_t* counts, float* bias,
                              void* stream) {
-  moe_status_t st = moe_check_cfg(cfg);
-  if (st != MOE_OK) return st;
+  // The sign rule reads E, K, T and gamma only: the whole-batch T of
+  // data-parallel replicas may exceed what one routing call accepts.
+  if (cfg == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cfg->E < 1 || cfg->K < 1 || cfg->K > cfg->E || cfg->T < 1 || !(cfg->gamma == cfg->gamma))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->E > 1024 || cfg->K > 32) return MOE_ERR_SHAPE;
   if (counts == nullptr || bias == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned16(counts) || !aligned16(bias)) return MOE_ERR_ALIGN;
   return from_cuda(launch_bias_update(*cfg, counts, bias, as_stream(stream)));

@@ -240,14 +240,9 @@ size_t router_tc_scratch_bytes(const moe_cfg_t& c) {
 cudaError_t launch_router_tc(const moe_cfg_t& c, const void* x, const float* w, float* affinity,
                              void* scratch, cudaStream_t st) {
   using namespace routertc;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const cudaError_t ea = ensure_smem_limit(reinterpret_cast<const void*>(router_tc_kernel),
+                                           static_cast<int>(kSmemBytes));
+  if (ea != cudaSuccess) return ea;
   // The split count is fixed (148 SMs of a B300) so that the scratch size
   // is a function of the shape alone.
   const int splits = router_splits(c, 148);
