@@ -239,6 +239,11 @@ moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y_perm,
  *   b_i <- fl32(b_i - gamma) if counts_i * E > T * K   (overloaded)
  *   b_i <- fl32(b_i + gamma) otherwise
  *   counts [E] int32 (from moe_route), bias [E] fp32 in/out.
+ * Only E, K, T and gamma are read, and only these are checked: 1 <= E <=
+ * 1024, 1 <= K <= min(32, E), T >= 1, gamma not NaN (MOE_ERR_INVALID_ARG /
+ * MOE_ERR_SHAPE otherwise; pointers are checked after the shape).  T may
+ * exceed moe_route's limit of 2^22 tokens: data-parallel replicas pass the
+ * whole batch, world size x T, with counts summed over the replicas.
  */
 moe_status_t moe_bias_update(const moe_cfg_t* cfg, const int32_t* counts,
                              float* bias, void* stream);

@@ -191,3 +191,30 @@ def test_backward_calls_check_before_launching():
     big = moe.moe_workspace_bytes(_base())
     assert lib.moe_experts_grouped_train(bf, *p, big, a, ws - 1, None) == 7
     assert lib.moe_experts_grouped_train(fp32, *p, big, a, ws, None) == 2
+
+
+def test_bias_update_takes_the_whole_batch_of_many_replicas():
+    """Data-parallel replicas call moe_bias_update with T = world x T (the
+    whole batch's mean load).  That T may exceed the 2^22 tokens one routing
+    call accepts: the bias update checks only E, K, T and gamma, so such a
+    configuration gets past the shape check to the pointer check (NULL
+    counts: MOE_ERR_INVALID_ARG, nothing launched)."""
+    from mixture_experts_layer_82_b300.replicas import global_cfg
+
+    lib = moe.library()
+    a = 0x100000
+    cfg = _base()
+    for world in (2, 64, 512):
+        g = global_cfg(cfg, world)
+        g.T = (1 << 22) + 1 if world == 2 else g.T * 600
+        assert moe.moe_check_cfg(g) != 0  # routing would refuse this T
+        assert lib.moe_bias_update(ctypes.byref(g.c()), None, a, None) == 1
+        assert lib.moe_bias_update(ctypes.byref(g.c()), a, a + 4, None) == 3
+    bad = _base()
+    bad.k = bad.E + 1
+    assert lib.moe_bias_update(ctypes.byref(bad.c()), a, a, None) == 1
+    bad = _base()
+    bad.E = 2048
+    bad.n_groups = 1
+    bad.topk_groups = 1
+    assert lib.moe_bias_update(ctypes.byref(bad.c()), a, a, None) == 2
