@@ -122,7 +122,7 @@ class MoELayer:
                     stream=stream)
         if update_bias:
             if load_group is not None:
-                world = global_load(self.counts, load_group)
+                world = global_load(self.counts, load_group, stream=stream)
                 moe_bias_update(global_cfg(c, world), self.counts, self.bias, stream=stream)
             else:
                 moe_bias_update(c, self.counts, self.bias, stream=stream)

@@ -16,12 +16,25 @@ from __future__ import annotations
 import copy
 
 
-def global_load(counts, group=None):
+def global_load(counts, group=None, stream=None):
     """Sums ``counts`` (the per-expert loads of this replica's batch) over
-    the replicas of ``group`` in place; returns the number of replicas."""
+    the replicas of ``group`` in place; returns the number of replicas.
+
+    ``stream`` (device tensors): the stream the routing that wrote
+    ``counts`` was enqueued on (a torch.cuda.Stream or a raw handle; None is
+    torch's current stream).  The all-reduce is issued with that stream
+    current, so that it reads the loads after the routing and the bias
+    update enqueued next on it reads the sums."""
+    import torch
     import torch.distributed as dist
 
-    dist.all_reduce(counts, op=dist.ReduceOp.SUM, group=group)
+    if counts.is_cuda and stream is not None:
+        if not isinstance(stream, torch.cuda.Stream):
+            stream = torch.cuda.ExternalStream(int(stream), device=counts.device)
+        with torch.cuda.stream(stream):
+            dist.all_reduce(counts, op=dist.ReduceOp.SUM, group=group)
+    else:
+        dist.all_reduce(counts, op=dist.ReduceOp.SUM, group=group)
     return dist.get_world_size(group)
 
 
