@@ -17,7 +17,7 @@ import torch
 import oracle
 import mixture_experts_layer_82_b300 as moe
 from moe_synth import CONFIGS, make_grad, make_layer, shape_with
-from helpers import ExpertView, host, rel_frobenius
+from helpers import ExpertView, assert_close, host, rel_frobenius
 
 pytestmark = pytest.mark.gpu
 
@@ -77,20 +77,20 @@ def test_backward_matches_oracle(shape):
                                   ExpertView(L["w2"]), ws13, ws2, fwd, host(dout),
                                   route_scale=shape.route_scale, affinity32=s32,
                                   y_perm=host(layer.y_perm))
-    assert rel_frobenius(host(layer.dgate), r["dgate"]) < TOL_F32
-    assert rel_frobenius(host(layer.dlogit), r["dlogit"]) < TOL_F32
-    assert rel_frobenius(host(layer.dy_perm), r["dy_perm"]) < TOL_BF16
-    assert rel_frobenius(host(layer.dx_perm), r["dx_perm"]) < TOL_BF16
-    assert rel_frobenius(host(layer.dx), r["dx"]) < TOL_BF16
-    assert rel_frobenius(host(layer.drouter_w), r["drouter_w"]) < TOL_BF16
-    assert rel_frobenius(host(layer.dw13), r["dw13"]) < TOL_BF16
-    assert rel_frobenius(host(layer.dw2), r["dw2"]) < TOL_BF16
+    assert_close(host(layer.dgate), r["dgate"], TOL_F32)
+    assert_close(host(layer.dlogit), r["dlogit"], TOL_F32)
+    assert_close(host(layer.dy_perm), r["dy_perm"], TOL_BF16)
+    assert_close(host(layer.dx_perm), r["dx_perm"], TOL_BF16)
+    assert_close(host(layer.dx), r["dx"], TOL_BF16)
+    assert_close(host(layer.drouter_w), r["drouter_w"], TOL_BF16)
+    assert_close(host(layer.dw13), r["dw13"], TOL_BF16)
+    assert_close(host(layer.dw2), r["dw2"], TOL_BF16)
     counts = host(layer.counts)
     assert np.all(host(layer.dw13)[counts == 0] == 0) and np.all(host(layer.dw2)[counts == 0] == 0)
     if shape.n_shared:
-        assert rel_frobenius(host(layer.dx_shared), r["dx_shared"]) < TOL_BF16
-        assert rel_frobenius(host(layer.dws13), r["dws13"]) < TOL_BF16
-        assert rel_frobenius(host(layer.dws2), r["dws2"]) < TOL_BF16
+        assert_close(host(layer.dx_shared), r["dx_shared"], TOL_BF16)
+        assert_close(host(layer.dws13), r["dws13"], TOL_BF16)
+        assert_close(host(layer.dws2), r["dws2"], TOL_BF16)
 
 
 def test_backward_is_deterministic():
@@ -119,7 +119,7 @@ def test_kept_gate_up_products_match_recomputed():
     for k in ("y_perm", "y_shared"):
         assert torch.equal(getattr(layer, k), ref[k]), k
     for k in ("dx", "drouter_w", "dw13", "dw2", "dws13", "dws2"):
-        assert rel_frobenius(host(getattr(layer, k)), host(ref[k])) < 1e-3, k
+        assert_close(host(getattr(layer, k)), host(ref[k]), 1e-3, k)
 
 
 def test_gathering_forward_gives_the_same_backward():
@@ -161,10 +161,10 @@ def test_full_size_backward_on_samples():
 
     # gates -> logits on every token, from the device's dgate
     _, dl = oracle.gate_backward(s32, idx, shape.route_scale, host(layer.dgate))
-    assert rel_frobenius(host(layer.dlogit), dl) < TOL_F32
+    assert_close(host(layer.dlogit), dl, TOL_F32)
     # router weights on every expert
     dr = oracle.router_weight_grad(x, idx, host(layer.dlogit), E)
-    assert rel_frobenius(host(layer.drouter_w), dr) < TOL_F32
+    assert_close(host(layer.drouter_w), dr, TOL_F32)
 
     # combine backward on sampled tokens
     rng = np.random.default_rng(5)
@@ -172,9 +172,9 @@ def test_full_size_backward_on_samples():
     yrows = {int(r): host(layer.y_perm[int(r)]) for r in ros[toks].reshape(-1)}
     ros_s = ros[toks]
     dy_s, dg_s = oracle.combine_backward(go[toks], yrows, ros_s, gates[toks])
-    assert rel_frobenius(host(layer.dgate)[toks], dg_s) < TOL_F32
+    assert_close(host(layer.dgate)[toks], dg_s, TOL_F32)
     got = np.stack([[host(layer.dy_perm[int(r)]) for r in row] for row in ros_s])
-    assert rel_frobenius(got, dy_s) < TOL_BF16
+    assert_close(got, dy_s, TOL_BF16)
 
     # routed experts: the lightest non-empty, the median and the heaviest
     counts = np.diff(off)
@@ -188,12 +188,12 @@ def test_full_size_backward_on_samples():
         w2 = host(L["w2"][e])
         units = _sample_units(I, 8, e)
         r = oracle.swiglu_ffn_backward(u, w13[units], w13[I + units], w2[:, units], dy)
-        assert rel_frobenius(host(layer.dw2[e])[:, units], r["dw2"]) < TOL_BF16, e
-        assert rel_frobenius(host(layer.dw13[e])[units], r["dw1"]) < TOL_BF16, e
-        assert rel_frobenius(host(layer.dw13[e])[I + units], r["dw3"]) < TOL_BF16, e
+        assert_close(host(layer.dw2[e])[:, units], r["dw2"], TOL_BF16, e)
+        assert_close(host(layer.dw13[e])[units], r["dw1"], TOL_BF16, e)
+        assert_close(host(layer.dw13[e])[I + units], r["dw3"], TOL_BF16, e)
         if hi - lo <= 256:  # the whole FFN for the input gradient of a short segment
             full = oracle.swiglu_ffn_backward(u, w13[:I], w13[I:], w2, dy)
-            assert rel_frobenius(host(layer.dx_perm[lo:hi]), full["du"]) < TOL_BF16, e
+            assert_close(host(layer.dx_perm[lo:hi]), full["du"], TOL_BF16, e)
 
     # shared expert: sampled hidden units over all tokens, input gradient of
     # sampled tokens
@@ -201,14 +201,14 @@ def test_full_size_backward_on_samples():
     w2 = host(L["ws2"][0])
     units = _sample_units(I, 8, 99)
     r = oracle.swiglu_ffn_backward(x, w13[units], w13[I + units], w2[:, units], go)
-    assert rel_frobenius(host(layer.dws2[0])[:, units], r["dw2"]) < TOL_BF16
-    assert rel_frobenius(host(layer.dws13[0])[units], r["dw1"]) < TOL_BF16
-    assert rel_frobenius(host(layer.dws13[0])[I + units], r["dw3"]) < TOL_BF16
+    assert_close(host(layer.dws2[0])[:, units], r["dw2"], TOL_BF16)
+    assert_close(host(layer.dws13[0])[units], r["dw1"], TOL_BF16)
+    assert_close(host(layer.dws13[0])[I + units], r["dw3"], TOL_BF16)
     full = oracle.swiglu_ffn_backward(x[toks], w13[:I], w13[I:], w2, go[toks])
-    assert rel_frobenius(host(layer.dx_shared)[toks], full["du"]) < TOL_BF16
+    assert_close(host(layer.dx_shared)[toks], full["du"], TOL_BF16)
 
     # the input gradient of sampled tokens from the device's expert parts
     dxp = {int(r): host(layer.dx_perm[int(r)]) for r in ros_s.reshape(-1)}
     dx_s = oracle.input_grad(host(layer.dx_shared)[toks], dxp, ros_s, idx[toks],
                              host(layer.dlogit)[toks], host(L["router_w"]))
-    assert rel_frobenius(host(layer.dx)[toks], dx_s) < TOL_BF16
+    assert_close(host(layer.dx)[toks], dx_s, TOL_BF16)

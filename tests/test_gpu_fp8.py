@@ -13,7 +13,7 @@ import torch
 import oracle
 import mixture_experts_layer_82_b300 as moe
 from moe_synth import CONFIGS, make_layer, shape_with
-from helpers import rel_frobenius, host, ExpertView
+from helpers import assert_close, host, ExpertView, tail_sample
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +35,13 @@ SHAPES = [
     # one token
     shape_with(CONFIGS["v3_fp8"], T=1, d=1024, E=16, n_groups=4, topk_groups=2, k=3,
                inter=512, router="gaussian", outlier_channels=10),
+    # the mid-size layer's widths in FP8, whole batch: 384 rows per expert on
+    # average, so a persistent CTA cycles its TMEM partials over several M
+    # tiles of one expert and most segments end in a ragged tile inside a
+    # multi-tile expert; two shared experts; 1% outlier channels
+    shape_with(CONFIGS["v3_fp8"], T=4096, d=2048, E=64, n_groups=8, topk_groups=4, k=6,
+               n_shared=2, inter=1408, route_scale=1.0, router="gaussian",
+               outlier_channels=20),
 ]
 
 
@@ -84,30 +91,33 @@ def test_fp8_layer_matches_oracle(shape):
                                      affinity32=host(aff))
     assert np.array_equal(host(layer.topk_idx), r["topk_idx"])
     assert np.array_equal(host(layer.offsets), r["offsets"])
-    assert rel_frobenius(host(layer.y_perm), r["y_perm"]) < TOL_FP8
+    assert_close(host(layer.y_perm), r["y_perm"], TOL_FP8)
     if shape.n_shared:
-        assert rel_frobenius(host(layer.y_shared), r["y_shared"]) < TOL_FP8
-    err = rel_frobenius(host(out), r["out"])
-    assert err < TOL_FP8, err
+        assert_close(host(layer.y_shared), r["y_shared"], TOL_FP8)
+    assert_close(host(out), r["out"], TOL_FP8)
 
 
 def test_fp8_full_size_layer_on_sampled_tokens():
     """The FP8 layer at its full size (T = 8192, d = 7168, 256 experts), in
-    the launch configuration the benchmark times; the oracle recomputes a
-    sample of tokens, quantising the master weights itself."""
+    the launch configuration the benchmark times; the oracle recomputes 64
+    tokens, quantising the master weights itself.  The sample holds the
+    tokens of the ragged last tile of the most loaded expert and the last
+    rows of one-tile and few-tile experts; each token's row is checked on
+    its own."""
     shape = CONFIGS["v3_fp8"]
     L, cfg, layer = _fp8_layer(shape)
     out = layer.forward(L["x"], update_bias=False)
     assert moe.moe_get_device_error() == 0
     o = host(out)
     assert np.all(np.isfinite(o))
-    rows = np.array([0, 2711, 5003, shape.T - 1])
+    rows = tail_sample(host(layer.offsets), host(layer.token_of_row), shape.T, 64)
+    assert len(rows) >= 64
     idx = host(layer.topk_idx)[rows]
     g = host(layer.topk_w)[rows].astype(np.float64)
     ref = oracle.moe_layer_tokens_fp8(host(L["x"][torch.tensor(rows, device=DEV)]), idx, g,
                                       ExpertView(L["w13"]), ExpertView(L["w2"]),
                                       ExpertView(L["ws13"]), ExpertView(L["ws2"]))
-    assert rel_frobenius(o[rows], ref) < TOL_FP8
+    assert_close(o[rows], ref, TOL_FP8)
 
 
 def test_fp8_layer_is_deterministic():

@@ -502,3 +502,50 @@ def test_sequence_balance_splits_sequences():
     fb, Pb, lb = oracle.sequence_balance(s[20:], idx[20:], 20)
     np.testing.assert_array_equal(f, np.concatenate([fa, fb]))
     np.testing.assert_array_equal(loss, np.concatenate([la, lb]))
+
+
+def test_fp8_sampled_tokens_match_whole_fp8_layer():
+    """The FP8 oracle's few-token form (the checker of the full-size FP8
+    layer) against the rows of its whole-layer form, on a tiny FP8 layer with
+    16 experts, top-3 and a shared expert: the per-token 1 x 128 tiles, the
+    per-expert weight blocks, the gate column of each slot and the shared
+    expert must all line up, so the rows agree to fp64 rounding."""
+    from oracle import moe_fp8
+    shape = shape_with(CONFIGS["v3_fp8"], T=24, d=256, E=16, n_groups=4, topk_groups=2, k=3,
+                       inter=128, router="gaussian", outlier_channels=3)
+    L = make_layer(shape, "cpu")
+    f = lambda t: t.float().numpy()
+    ins = [f(L[k]) for k in ("x", "router_w", "bias", "w13", "w2", "ws13", "ws2")]
+    r = moe_fp8.moe_layer_forward_fp8(*ins, n_groups=shape.n_groups,
+                                      topk_groups=shape.topk_groups, k=shape.k,
+                                      route_scale=shape.route_scale)
+    assert len(set(r["topk_idx"].reshape(-1).tolist())) >= 8   # many experts in play
+    rows = [0, 5, 11, 23]
+    y = moe_fp8.moe_layer_tokens_fp8(ins[0][rows], r["topk_idx"][rows], r["topk_w"][rows],
+                                     ins[3], ins[4], ins[5], ins[6])
+    np.testing.assert_allclose(y, r["out"][rows], rtol=1e-12, atol=1e-12)
+    # a slot's gate belongs to that slot's expert: swapping two gate columns
+    # of a token changes its row
+    g = r["topk_w"][rows].copy()
+    g[:, [0, 1]] = g[:, [1, 0]]
+    y2 = moe_fp8.moe_layer_tokens_fp8(ins[0][rows], r["topk_idx"][rows], g,
+                                      ins[3], ins[4], ins[5], ins[6])
+    assert np.max(np.abs(y2 - r["out"][rows])) > 1e-3
+
+
+def test_load_spread_hand_example():
+    """Loads [0, 2, 4, 6] over four experts: mean 3, max / mean = 2,
+    population standard deviation sqrt((9 + 1 + 1 + 9) / 4) = sqrt(5), so the
+    coefficient of variation is sqrt(5) / 3; min 0, max 6.  An even load
+    gives max / mean = 1 and CV = 0."""
+    s = oracle.load_spread(np.array([0, 2, 4, 6]))
+    assert s["max_over_mean"] == 2.0
+    assert abs(s["cv"] - np.sqrt(5.0) / 3.0) < 1e-15
+    assert (s["min"], s["max"]) == (0, 6)
+    e = oracle.load_spread(np.full(8, 5))
+    assert (e["max_over_mean"], e["cv"], e["min"], e["max"]) == (1.0, 0.0, 5, 5)
+    # the benchmark's host-side report of the same loads (T * K = 12 selections)
+    import bench
+    b = bench.load_stats([0, 2, 4, 6], T=4, K=3)
+    assert b["max_over_mean"] == 2.0 and abs(b["cv"] - np.sqrt(5.0) / 3.0) < 1e-15
+    assert (b["min"], b["max"], b["empty_experts"]) == (0, 6, 1)
