@@ -1,15 +1,18 @@
 """Benchmark of the DeepSeekMoE layer forward on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload v3_bf16|v3_fp8|v3_decode|mid_bf16]
+                    [--workload v3_bf16|v3_fp8|v3_decode|mid_bf16] [--no-also]
 
 A step is one pass of the whole layer (route -> permute -> grouped expert
 GEMMs -> combine -> bias update) over one batch of T tokens, with every
 input already resident in device memory.  The default workload is the
 DeepSeek-V3-shaped layer in bf16 (T=8192, d=7168, 256 routed experts in 8
 groups, top-4 groups, top-8, 1 shared expert, I=2048, route scale 2.5, Zipf
--skewed router).  With N > 1 (torchrun) every rank runs its own replica on
-its own batch (weak scaling, no collective on the data path; the replicas
+-skewed router); the same run also times the FP8 layer of that shape and
+the decode-shaped batch (T=128) and reports them under "also", each with
+its own roofline, clock record and end-to-end figure.  With N > 1
+(torchrun) every rank runs its own replica on its own batch (weak scaling,
+no collective on the data path; the replicas
 sum their per-expert loads with one all-reduce of counts[E] per step so that
 the bias update sees the whole batch); the time is the maximum over ranks.
 Rank 0 prints one JSON line.
@@ -412,7 +415,30 @@ def run_reference(args, shape, world, rank):
     return 0
 
 
+ALSO = ("v3_fp8", "v3_decode")  # timed beside the default workload in the same run
+
+
 def run_ours(args, shape, world, rank, local):
+    """The headline line; with the default workload (and no --no-also) the
+    FP8 and decode-shaped V3 layers are timed in the same run and reported
+    under "also", each with its own roofline, clocks and e2e."""
+    line = measure_ours(args, shape, world, rank, local, cpu_baseline=True)
+    if args.workload == "v3_bf16" and not args.set and not args.no_also:
+        line["also"] = {}
+        for name in ALSO:
+            sub = measure_ours(args, CONFIGS[name], world, rank, local, cpu_baseline=False)
+            for k in ("metric", "n_gpus", "steps", "warmup", "higher_is_better", "scaling",
+                      "vs_baseline", "data"):
+                sub.pop(k, None)
+            line["also"][name] = sub
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def measure_ours(args, shape, world, rank, local, cpu_baseline):
+    """Times one workload: device-resident steps (CUDA events), then the same
+    steps end to end through host buffers; returns the JSON line's fields."""
     import mixture_experts_layer_82_b300 as moe
 
     dev = f"cuda:{local}"
@@ -580,15 +606,17 @@ def run_ours(args, shape, world, rank, local):
     }
     if shape.bias_steps:
         line["load_balance"] = load_balance(moe, shape, L, shape.bias_steps)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if cpu_baseline and rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs, n = oracle_sample(shape, L, args.cpu_tokens)
         line["cpu_baseline"] = {
             "value": n / secs, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"{n} tokens of the same batch end to end through the fp64 oracle "
                       f"({secs:.1f} s)"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    return 0
+    # release this workload's weights and buffers before the next one
+    del layer, L, x, x_host, x_dev, out_dev, out_host
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
 
 
 def run_train(args, shape, world, rank, local):
@@ -742,6 +770,9 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", action="store_true",
+                    help="with the default workload, time it alone (without the FP8 and "
+                         "decode-shaped layers reported under \"also\")")
     ap.add_argument("--dispatch", choices=["permute", "gather"], default="permute",
                     help="bf16 kind: permute x into per-expert rows before the expert GEMMs, "
                          "or gather the rows inside the gate/up GEMM")
