@@ -197,36 +197,35 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int 
 }
 
 // Scales of the epilogue thread's row and columns, K block after K block.
-// Activation: sa[row, kb] (0 for a row past the segment).  Gate/up: the
-// W1 block and the matching W3 block of the tile's 128 h columns.  Down:
-// the thread's 128-column block of W2 (0 for a block past d); the shared
-// class walks K over its N_s matrices, so the cursor steps to the next
-// matrix every I/128 blocks.  Loads are issued two K blocks before use.
+// Activation: sa[row, kb] (a row past the segment reads the segment's first
+// row: its sums are never stored).  Gate/up: the W1 block and the matching
+// W3 block of the tile's 128 h columns (the W3 block row lies `up` floats
+// after the W1 one).  Down: the thread's 128-column block of W2 (0 for a
+// block past d); the shared class walks K over its N_s matrices, so the
+// cursor steps to the next matrix every I/128 blocks.  Loads are issued two
+// K blocks before use.
 template <int MODE>
 struct ScaleCursor {
   const float* a;   // activation scales of the row, next block to load
-  const float* w0;  // gate/up: W1 block row; down: W2 block at kl = 0 of the current matrix
-  const float* w1;  // gate/up: W3 block row
-  int kl;           // next K block (gate/up: absolute; down: inside the current matrix)
+  const float* w;   // gate/up: W1 block of the next block; down: W2 block at kl = 0 of the current matrix
+  int up;           // gate/up: floats from a W1 block to the matching W3 block
+  int kl;           // down: next K block inside the current matrix
   int kbs;          // down: K blocks per matrix
   int mat_floats;   // down: scale floats per matrix
-  bool row_ok, col_ok;
+  bool col_ok;      // down: the column block lies inside d
 
-  __device__ __forceinline__ void init(const Params& p, const Tile& tl, int hf, bool valid,
-                                       size_t grow) {
+  __device__ __forceinline__ void init(const Params& p, const Tile& tl, int hf, size_t grow) {
     const ClassDesc& cd = p.cls[tl.cls];
     const int I = p.inter;
     a = cd.a_scales + grow * (cd.k_dim / BK);
-    row_ok = valid;
     kl = 0;
     if (MODE == GATEUP) {
       const int n0 = tl.nt * (BN / 2);
       const int mat = tl.cls == 0 ? tl.group : n0 / I;
       const int i0 = n0 % I;
       const int kd = p.d / BK, nbs = 2 * I / BK;
-      const float* base = cd.w_scales + static_cast<size_t>(mat) * nbs * kd;
-      w0 = base + static_cast<size_t>(i0 / BK) * kd;
-      w1 = base + static_cast<size_t>((I + i0) / BK) * kd;
+      w = cd.w_scales + (static_cast<size_t>(mat) * nbs + i0 / BK) * kd;
+      up = (I / BK) * kd;
       col_ok = true;
     } else {
       const int nbs = p.d / BK;
@@ -235,23 +234,22 @@ struct ScaleCursor {
       mat_floats = nbs * kbs;
       col_ok = nb < nbs;
       const int mat = tl.cls == 0 ? tl.group : 0;
-      w0 = cd.w_scales + (static_cast<size_t>(mat) * nbs + (col_ok ? nb : 0)) * kbs;
-      w1 = w0;
+      w = cd.w_scales + (static_cast<size_t>(mat) * nbs + (col_ok ? nb : 0)) * kbs;
     }
   }
 
   // Loads the next K block's scales and advances.
   __device__ __forceinline__ void next(float& sa, float& s0, float& s1) {
-    sa = row_ok ? __ldg(a) : 0.f;
+    sa = __ldg(a);
     ++a;
     if (MODE == GATEUP) {
-      s0 = __ldg(w0 + kl);
-      s1 = __ldg(w1 + kl);
-      ++kl;
+      s0 = __ldg(w);
+      s1 = __ldg(w + up);
+      ++w;
     } else {
-      s0 = col_ok ? __ldg(w0 + kl) : 0.f;
+      s0 = col_ok ? __ldg(w + kl) : 0.f;
       s1 = 0.f;
-      if (++kl == kbs) { kl = 0; w0 += mat_floats; }
+      if (++kl == kbs) { kl = 0; w += mat_floats; }
     }
   }
 };
@@ -275,7 +273,7 @@ __device__ __forceinline__ bool promote_block(Smem& s, float (&acc)[128], uint32
   // partial goes back to the MMA issuer as soon as the last batch is in
   // registers (tcgen05.wait::ld returns once the loads have completed),
   // before that batch's FMAs.
-  constexpr int NB = MODE == GATEUP ? 4 : 2;  // batches
+  constexpr int NB = 2;  // batches
   constexpr int W = 128 / (2 * NB);           // columns per load
 #pragma unroll
   for (int r = 0; r < NB; ++r) {
@@ -475,8 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
         const Tile tl = decode_tile<MODE>(p, s, t, gh);
         nk = p.cls[tl.cls].k_dim / BK;
         const int m = tl.mt * BM + r_in_tile;
-        const bool valid = m < tl.rows;
-        sc.init(p, tl, hf, valid, static_cast<size_t>(tl.row0) + (valid ? m : 0));
+        sc.init(p, tl, hf, static_cast<size_t>(tl.row0) + (m < tl.rows ? m : 0));
       }
       float acc[128];
 #pragma unroll
