@@ -553,16 +553,26 @@ cudaError_t launch_experts_bwd_input_bf16(const ExpertsBwdArgs& a, cudaStream_t 
     g.offsets = a.offsets; g.n_rows = static_cast<int>(tk); g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
     g.d = 2 * I;   // B rows of one routed matrix
     g.inter = d;   // K of one matrix
+    // (each map also with half its box: the kernel runs in CTA pairs that
+    // split and share one operand of two tiles)
     CUresult r = encode_bf16_2d(&g.a_map[0], a.x_perm, d, tk, BK, BM);
+    if (r == CUDA_SUCCESS) r = encode_bf16_2d(&g.a_half[0], a.x_perm, d, tk, BK, BM / 2);
     if (r == CUDA_SUCCESS)
       r = encode_bf16_2d(&g.b_map[0], a.w13, d, static_cast<uint64_t>(c.E) * 2 * I, BK, BN);
+    if (r == CUDA_SUCCESS)
+      r = encode_bf16_2d(&g.b_half[0], a.w13, d, static_cast<uint64_t>(c.E) * 2 * I, BK, BN / 2);
     if (r == CUDA_SUCCESS && has_shared) {
       r = encode_bf16_2d(&g.a_map[1], a.x, d, c.T, BK, BM);
+      if (r == CUDA_SUCCESS) r = encode_bf16_2d(&g.a_half[1], a.x, d, c.T, BK, BM / 2);
       if (r == CUDA_SUCCESS)
         r = encode_bf16_2d(&g.b_map[1], a.ws13, d, static_cast<uint64_t>(Ns) * 2 * I, BK, BN);
+      if (r == CUDA_SUCCESS)
+        r = encode_bf16_2d(&g.b_half[1], a.ws13, d, static_cast<uint64_t>(Ns) * 2 * I, BK, BN / 2);
     } else {
       g.a_map[1] = g.a_map[0];
       g.b_map[1] = g.b_map[0];
+      g.a_half[1] = g.a_half[0];
+      g.b_half[1] = g.b_half[0];
     }
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     g.cls[0] = ClassDesc{w.ab, 2 * I, 2 * I, d};

@@ -10,11 +10,23 @@
 //            epilogue (the tile's 256 MMA columns are 128 gate rows and the
 //            128 matching up rows of W13, so a tile yields 128 h columns);
 //   down:    y = h W2^T per 128 x 256 tile.
-// The work list is every (group, M tile, N tile) of the routed experts
+// The work list covers every (group, M tile, N tile) of the routed experts
 // (segment sizes read from `offsets` in device memory) followed by the
-// shared class (all T rows, intermediate N_s * I).  CTA i takes tiles
-// i, i + grid, ...; inside a group the M tile varies fastest, so the CTAs
-// running at the same time share each weight tile through L2.
+// shared class (all T rows, intermediate N_s * I).  The CTAs run in
+// clusters of two, and a cluster's unit of work is a pair of tiles that
+// share one operand, loaded once from L2 and multicast into both CTAs:
+//   - two M tiles of one group with the same weight (B) tile: each CTA
+//     loads its own A rows and half of the B tile for both;
+//   - the odd last M tile of a group with two of its N tiles: each CTA
+//     loads half of the A rows for both and its own B tile;
+//   - an odd last (M, N) tile, paired with an empty tile past the segment.
+// Each CTA still holds whole A and B tiles and runs its own 128 x 256 MMAs;
+// what the pair saves is L2 -> shared-memory traffic, which bounds these
+// GEMMs (a stage moves 48 KiB per 512 MMA cycles; sharing B makes it
+// 32 KiB per CTA).  Cluster c takes units c, c + clusters, ...; inside a
+// group the M pair varies fastest, so the clusters running at the same time
+// share each weight tile through L2.  (The gathering gate/up GEMM keeps one
+// tile per CTA: its A rows come from gather warps, not TMA.)
 //
 // Roles (224 threads, one CTA per SM):
 //   warps 0, 6  TMA producers (even / odd stages): A and B tiles into a
@@ -28,6 +40,8 @@
 // error word and a block-wide abort flag so that all roles leave, drain
 // their own copies in flight and free TMEM.
 #include <algorithm>
+#include <map>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -47,8 +61,11 @@ constexpr int THREADS_GATHER = THREADS + STAGES * 32;
 constexpr int MAX_GROUPS = 1025;             // 1024 routed experts + the shared class
 constexpr uint32_t TMEM_COLS = 512;          // two 256-column accumulators
 constexpr uint32_t IDESC = idesc_f32acc(1, 1, BM, BN);
+constexpr uint16_t kPairMask = 0x3;          // both CTAs of a cluster
 
 enum { GATEUP = 0, DOWN = 1 };
+// Operand a pair unit's two tiles share.
+enum { SHARE_B = 0, SHARE_A = 1 };
 
 struct ClassDesc {
   __nv_bfloat16* out;  // output rows of the class
@@ -60,8 +77,10 @@ struct ClassDesc {
 };
 
 struct Params {
-  CUtensorMap a_map[2];  // [0] routed rows, [1] shared rows
-  CUtensorMap b_map[2];  // [0] routed weights, [1] shared weights
+  CUtensorMap a_map[2];   // [0] routed rows, [1] shared rows: 128-row box
+  CUtensorMap b_map[2];   // [0] routed weights, [1] shared weights: whole B tile
+  CUtensorMap a_half[2];  // the same A with a 64-row box (units sharing A)
+  CUtensorMap b_half[2];  // the same B with a half-tile box (units sharing B)
   ClassDesc cls[2];
   const int32_t* offsets;
   int n_rows;  // T * K: permuted rows, the bound of every segment
@@ -95,6 +114,7 @@ constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(Smem);
 static_assert(kSmemBytes <= 232448, "above the 227 KiB of shared memory a block may use");
 
 struct Tile {
+  int share;    // pair units: SHARE_B or SHARE_A
   int cls;      // 0 routed, 1 shared
   int group;    // routed expert index (cls 0)
   int row0;     // first row of the group in its class's row space
@@ -110,8 +130,16 @@ __device__ __forceinline__ int n_tiles_of(const Params& p, int cls) {
   return ceil_div(p.cls[cls].n_out, out_tile_cols<MODE>());
 }
 
-// Warp-cooperative build of the tile table from the segment offsets.
-template <int MODE>
+// Pair units of a group of mt M tiles and nt N tiles: M pairs sharing a B
+// tile, then, for an odd last M tile, N pairs sharing its A rows (an odd
+// last N tile pairs with an empty tile).
+__device__ __forceinline__ int pair_units(int mt, int nt) {
+  return (mt / 2) * nt + (mt & 1) * ((nt + 1) / 2);
+}
+
+// Warp-cooperative build of the work table from the segment offsets:
+// first work item (tile, or pair unit) of every group.
+template <int MODE, bool PAIR>
 __device__ void build_tile_table(const Params& p, Smem& s) {
   const int lane = threadIdx.x % 32;
   const int G = p.E + (p.has_shared ? 1 : 0);
@@ -131,7 +159,8 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
     }
     const int mt = ceil_div(max(rows, 0), BM);
     s.mtiles[g] = mt;
-    sum += mt * n_tiles_of<MODE>(p, cls);
+    const int nt = n_tiles_of<MODE>(p, cls);
+    sum += PAIR ? pair_units(mt, nt) : mt * nt;
   }
   int incl = sum;
 #pragma unroll
@@ -142,8 +171,8 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
   int run = incl - sum;
   for (int g = g0; g < g1; ++g) {
     s.gstart[g] = run;
-    const int cls = g < p.E ? 0 : 1;
-    run += s.mtiles[g] * n_tiles_of<MODE>(p, cls);
+    const int nt = n_tiles_of<MODE>(p, g < p.E ? 0 : 1);
+    run += PAIR ? pair_units(s.mtiles[g], nt) : s.mtiles[g] * nt;
   }
   if (lane == 31) {
     s.gstart[G] = incl;
@@ -152,8 +181,9 @@ __device__ void build_tile_table(const Params& p, Smem& s) {
   }
 }
 
-template <int MODE>
-__device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int t) {
+// This CTA's tile of work item t (rank: the CTA's rank in its cluster).
+template <int MODE, bool PAIR>
+__device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int t, int rank) {
   int lo = 0, hi = s.n_groups;  // gstart[lo] <= t < gstart[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -164,8 +194,28 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int 
   tl.group = lo;
   const int local = t - s.gstart[lo];
   const int mt_count = s.mtiles[lo];
-  tl.mt = local % mt_count;
-  tl.nt = local / mt_count;
+  tl.share = SHARE_B;
+  if (!PAIR) {
+    tl.mt = local % mt_count;
+    tl.nt = local / mt_count;
+  } else {
+    const int nt_count = n_tiles_of<MODE>(p, tl.cls);
+    const int pm = mt_count / 2;
+    if (local < pm * nt_count) {
+      tl.nt = local / pm;
+      tl.mt = 2 * (local % pm) + rank;
+    } else {
+      const int l2 = local - pm * nt_count;
+      tl.mt = mt_count - 1;
+      if (2 * l2 + 1 < nt_count) {
+        tl.share = SHARE_A;
+        tl.nt = 2 * l2 + rank;
+      } else {
+        tl.nt = nt_count - 1;
+        tl.mt += rank;  // the partner of an odd last tile: no rows, nothing stored
+      }
+    }
+  }
   if (tl.cls == 0) { tl.row0 = s.off[lo]; tl.rows = s.off[lo + 1] - tl.row0; }
   else { tl.row0 = 0; tl.rows = p.T; }
   return tl;
@@ -174,6 +224,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Smem& s, int 
 template <int MODE, bool GATHER>
 __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
     experts_bf16_kernel(const __grid_constant__ Params p) {
+  constexpr bool PAIR = !GATHER;  // launched in clusters of two
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -182,10 +233,20 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
   volatile int* abort_flag = &s.abort;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) { tma_prefetch_desc(&p.a_map[i]); tma_prefetch_desc(&p.b_map[i]); }
-    // a stage is full once the producer's TMA bytes have landed and, when
-    // gathering, the slot's gather warp has arrived
-    for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], GATHER ? 2 : 1); mbar_init(&s.empty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      tma_prefetch_desc(&p.a_map[i]);
+      tma_prefetch_desc(&p.b_map[i]);
+      if (PAIR) { tma_prefetch_desc(&p.a_half[i]); tma_prefetch_desc(&p.b_half[i]); }
+    }
+    // a stage is full once the producer's TMA bytes have landed (in a pair,
+    // also the partner's multicast half) and, when gathering, the slot's
+    // gather warp has arrived; it is empty again once the MMAs of this CTA
+    // and, in a pair, of the partner (whose copy of the slot the multicast
+    // also writes) have read it
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&s.full[i], GATHER ? 2 : 1);
+      mbar_init(&s.empty[i], PAIR ? 2 : 1);
+    }
     for (int i = 0; i < 2; ++i) { mbar_init(&s.tfull[i], 1); mbar_init(&s.tempty[i], 4); }
     mbar_init(&s.done, 1);
     s.abort = 0;
@@ -196,11 +257,17 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
     tmem_relinquish();
     tc_fence_before();
   }
-  if (warp == 2) build_tile_table<MODE>(p, s);
+  if (warp == 2) build_tile_table<MODE, PAIR>(p, s);
   __syncthreads();
+  // both CTAs' barriers are initialised before either multicasts into the other
+  if (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_base;
   const int total = s.gstart[s.n_groups];
+  // work items: a cluster's pair units, or this CTA's tiles
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int w_first = PAIR ? static_cast<int>(blockIdx.x) >> 1 : static_cast<int>(blockIdx.x);
+  const int w_step = PAIR ? static_cast<int>(gridDim.x) >> 1 : static_cast<int>(gridDim.x);
 
   if (warp == 0 || warp == PRODUCER2) {
     // ----------------------------------------------------------- producers
@@ -214,8 +281,8 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
       uint32_t g = 0;     // stages of the CTA so far
       uint32_t mine = 0;  // stages issued by this thread
       bool stop = false;
-      for (int t = blockIdx.x; t < total && !stop && !*abort_flag; t += gridDim.x) {
-        const Tile tl = decode_tile<MODE>(p, s, t);
+      for (int t = w_first; t < total && !stop && !*abort_flag; t += w_step) {
+        const Tile tl = decode_tile<MODE, PAIR>(p, s, t, rank);
         const int nk = p.cls[tl.cls].k_dim / BK;
         const int a_row = tl.row0 + tl.mt * BM;
         const CUtensorMap* am = &p.a_map[tl.cls];
@@ -242,9 +309,28 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
             // gathering: the routed A rows come from the slot's gather warp
             const bool a_by_tma = !GATHER || tl.cls != 0;
             mbar_arrive_expect_tx(&s.full[stage], (a_by_tma ? A_BYTES : 0) + B_BYTES);
-            if (MODE == GATEUP) tma_load_4d(sb, bm, &s.full[stage], kb * BK, bi, 0, bmat, pol_b);
-            else tma_load_2d(sb, bm, &s.full[stage], bxk, brow, pol_b);
-            if (a_by_tma) tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
+            if (PAIR && tl.share == SHARE_B) {
+              // own A rows; this CTA's half of the common B tile, for both
+              // (gate/up: W1 rows from rank 0, the matching W3 rows from
+              // rank 1; down: the first or the second 128 rows)
+              tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
+              uint8_t* sbh = sb + rank * (B_BYTES / 2);
+              const CUtensorMap* bh = &p.b_half[tl.cls];
+              if (MODE == GATEUP)
+                tma_load_4d_mc(sbh, bh, &s.full[stage], kb * BK, bi, rank, bmat, kPairMask, pol_b);
+              else
+                tma_load_2d_mc(sbh, bh, &s.full[stage], bxk, brow + rank * (BN / 2), kPairMask, pol_b);
+            } else if (PAIR) {
+              // this CTA's half of the common A rows, for both; own B tile
+              tma_load_2d_mc(sa + rank * (A_BYTES / 2), &p.a_half[tl.cls], &s.full[stage], kb * BK,
+                             a_row + rank * (BM / 2), kPairMask, pol_a);
+              if (MODE == GATEUP) tma_load_4d(sb, bm, &s.full[stage], kb * BK, bi, 0, bmat, pol_b);
+              else tma_load_2d(sb, bm, &s.full[stage], bxk, brow, pol_b);
+            } else {
+              if (MODE == GATEUP) tma_load_4d(sb, bm, &s.full[stage], kb * BK, bi, 0, bmat, pol_b);
+              else tma_load_2d(sb, bm, &s.full[stage], bxk, brow, pol_b);
+              if (a_by_tma) tma_load_2d(sa, am, &s.full[stage], kb * BK, a_row, pol_a);
+            }
             ++mine;
           }
           if (MODE == DOWN) {
@@ -276,8 +362,8 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
     const int rsub = lane >> 3, c = lane & 7;  // 8 lanes cover one 128-byte row
     uint32_t g = 0;  // stages of the CTA so far
     bool stop = false;
-    for (int t = blockIdx.x; t < total && !stop && !*abort_flag; t += gridDim.x) {
-      const Tile tl = decode_tile<MODE>(p, s, t);
+    for (int t = w_first; t < total && !stop && !*abort_flag; t += w_step) {
+      const Tile tl = decode_tile<MODE, PAIR>(p, s, t, rank);
       const int nk = p.cls[tl.cls].k_dim / BK;
       const bool routed = tl.cls == 0;
       if (routed) {
@@ -320,8 +406,8 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool any = false;
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++it) {
-        const Tile tl = decode_tile<MODE>(p, s, t);
+      for (int t = w_first; t < total && !*abort_flag; t += w_step, ++it) {
+        const Tile tl = decode_tile<MODE, PAIR>(p, s, t, rank);
         const int nk = p.cls[tl.cls].k_dim / BK;
         const int acc = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
@@ -340,7 +426,9 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
                         IDESC, (kb | k) != 0 ? 1u : 0u);
           }
           any = true;
-          mma_commit(&s.empty[stage]);
+          // the slot is free again once both CTAs of a pair have read it
+          if (PAIR) mma_commit_mc(&s.empty[stage], kPairMask);
+          else mma_commit(&s.empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -357,8 +445,8 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r_in_tile = q * 32 + lane;
     int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const Tile tl = decode_tile<MODE>(p, s, t);
+    for (int t = w_first; t < total; t += w_step, ++it) {
+      const Tile tl = decode_tile<MODE, PAIR>(p, s, t, rank);
       const ClassDesc& cd = p.cls[tl.cls];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
@@ -429,6 +517,9 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
     }
   }
   __syncthreads();
+  // neither CTA of a pair leaves while the other may still multicast into
+  // it or arrive on its barriers
+  if (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -456,15 +547,67 @@ void experts_scratch_carve(const moe_cfg_t& c, void* ws, void** h, float** h_sca
     *h_scales = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(hr + hs, 256));
 }
 
+// Clusters of two CTAs that can be resident at once (one CTA per SM), per
+// (device, kernel).
+static int pair_clusters(const void* func, const cudaLaunchConfig_t& cfg) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> known;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = known.find({dev, func});
+  if (it != known.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sm_count() / 2;
+  }
+  n = std::min(n, sm_count() / 2);
+  known[{dev, func}] = n;
+  return n;
+}
+
 template <int MODE, bool GATHER>
 static cudaError_t launch_bf16_gemm(const bf16gemm::Params& prm, cudaStream_t st) {
   using namespace bf16gemm;
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(experts_bf16_kernel<MODE, GATHER>),
-                                    static_cast<int>(kSmemBytes));
+  const void* func = reinterpret_cast<const void*>(experts_bf16_kernel<MODE, GATHER>);
+  cudaError_t e = ensure_smem_limit(func, static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  experts_bf16_kernel<MODE, GATHER>
-      <<<sm_count(), GATHER ? THREADS_GATHER : THREADS, kSmemBytes, st>>>(prm);
-  return cudaGetLastError();
+  if (GATHER) {
+    experts_bf16_kernel<MODE, GATHER><<<sm_count(), THREADS_GATHER, kSmemBytes, st>>>(prm);
+    return cudaGetLastError();
+  }
+  // persistent clusters of two CTAs (pair units), as many as fit at once
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2);
+  cfg.gridDim = dim3(2 * pair_clusters(func, cfg));
+  e = cudaLaunchKernelEx(&cfg, experts_bf16_kernel<MODE, GATHER>, prm);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// A-like operand (rows of `inner` bf16 elements, 128-byte swizzle) encoded
+// twice: box of `rows` rows and of rows / 2 rows.
+static CUresult encode_bf16_pair(CUtensorMap* full, CUtensorMap* half, const void* base,
+                                 uint64_t inner, uint64_t outer, uint32_t rows) {
+  using namespace bf16gemm;
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  CUresult r = encode_tensor_map_2d(full, BF, const_cast<void*>(base), inner, outer, inner * 2, BK,
+                                    rows, SW);
+  if (r == CUDA_SUCCESS)
+    r = encode_tensor_map_2d(half, BF, const_cast<void*>(base), inner, outer, inner * 2, BK,
+                             rows / 2, SW);
+  return r;
 }
 
 cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
@@ -476,7 +619,6 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
   __nv_bfloat16* h_shared = h_routed + tk * I;
   const bool has_shared = Ns > 0;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
 
   // ---- gate/up: A = x_perm (or, gathering, x[token_of_row]) / x, B = W13
   const bool gather = a.token_of_row != nullptr;
@@ -486,18 +628,19 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
   g.token_of_row = a.token_of_row;
   g.x_rows = static_cast<const __nv_bfloat16*>(a.x);
   // (gathering never reads the routed A map; it is encoded over x to stay valid)
-  CUresult r = gather ? encode_tensor_map_2d(&g.a_map[0], BF, const_cast<void*>(a.x), c.d, c.T,
-                                             static_cast<uint64_t>(c.d) * 2, BK, BM, SW)
-                      : encode_tensor_map_2d(&g.a_map[0], BF, const_cast<void*>(a.x_perm), c.d, tk,
-                                             static_cast<uint64_t>(c.d) * 2, BK, BM, SW);
-  if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[0], BF, a.w13, c.E, I, c.d, 2, BK);
+  CUresult r = gather ? encode_bf16_pair(&g.a_map[0], &g.a_half[0], a.x, c.d, c.T, BM)
+                      : encode_bf16_pair(&g.a_map[0], &g.a_half[0], a.x_perm, c.d, tk, BM);
+  if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[0], BF, a.w13, c.E, I, c.d, 2, BK, 2);
+  if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_half[0], BF, a.w13, c.E, I, c.d, 2, BK, 1);
   if (r == CUDA_SUCCESS && has_shared) {
-    r = encode_tensor_map_2d(&g.a_map[1], BF, const_cast<void*>(a.x), c.d, c.T,
-                             static_cast<uint64_t>(c.d) * 2, BK, BM, SW);
-    if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[1], BF, a.ws13, Ns, I, c.d, 2, BK);
+    r = encode_bf16_pair(&g.a_map[1], &g.a_half[1], a.x, c.d, c.T, BM);
+    if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_map[1], BF, a.ws13, Ns, I, c.d, 2, BK, 2);
+    if (r == CUDA_SUCCESS) r = encode_gate_up_map(&g.b_half[1], BF, a.ws13, Ns, I, c.d, 2, BK, 1);
   } else {
     g.a_map[1] = g.a_map[0];
     g.b_map[1] = g.b_map[0];
+    g.a_half[1] = g.a_half[0];
+    g.b_half[1] = g.b_half[0];
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   g.cls[0] = ClassDesc{h_routed, I, I, c.d, a.ab, 2 * I};
@@ -507,22 +650,20 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
 
   // ---- down: A = h, B = W2
   Params dn = g;
-  r = encode_tensor_map_2d(&dn.a_map[0], BF, h_routed, I, tk, static_cast<uint64_t>(I) * 2, BK, BM,
-                           SW);
+  r = encode_bf16_pair(&dn.a_map[0], &dn.a_half[0], h_routed, I, tk, BM);
   if (r == CUDA_SUCCESS)
-    r = encode_tensor_map_2d(&dn.b_map[0], BF, const_cast<void*>(a.w2), I,
-                             static_cast<uint64_t>(c.E) * c.d, static_cast<uint64_t>(I) * 2, BK,
-                             BN, SW);
+    r = encode_bf16_pair(&dn.b_map[0], &dn.b_half[0], a.w2, I, static_cast<uint64_t>(c.E) * c.d, BN);
   if (r == CUDA_SUCCESS && has_shared) {
-    r = encode_tensor_map_2d(&dn.a_map[1], BF, h_shared, static_cast<uint64_t>(Ns) * I, c.T,
-                             static_cast<uint64_t>(Ns) * I * 2, BK, BM, SW);
+    r = encode_bf16_pair(&dn.a_map[1], &dn.a_half[1], h_shared, static_cast<uint64_t>(Ns) * I, c.T,
+                         BM);
     if (r == CUDA_SUCCESS)
-      r = encode_tensor_map_2d(&dn.b_map[1], BF, const_cast<void*>(a.ws2), I,
-                               static_cast<uint64_t>(Ns) * c.d, static_cast<uint64_t>(I) * 2, BK,
-                               BN, SW);
+      r = encode_bf16_pair(&dn.b_map[1], &dn.b_half[1], a.ws2, I, static_cast<uint64_t>(Ns) * c.d,
+                           BN);
   } else {
     dn.a_map[1] = dn.a_map[0];
     dn.b_map[1] = dn.b_map[0];
+    dn.a_half[1] = dn.a_half[0];
+    dn.b_half[1] = dn.b_half[0];
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   dn.cls[0] = ClassDesc{static_cast<__nv_bfloat16*>(a.y_perm), c.d, c.d, I};
