@@ -456,8 +456,9 @@ def measure_ours(args, shape, world, rank, local, cpu_baseline):
     if world > 1:
         import torch.distributed as dist
         lg = dist.group.WORLD
+    gated = args.gated and not gather
     for _ in range(args.warmup):
-        layer.forward(x, load_group=lg)
+        layer.forward(x, load_group=lg, gated=gated)
     torch.cuda.synchronize()
     status = moe.moe_get_device_error()
     if status != 0:
@@ -474,7 +475,7 @@ def measure_ours(args, shape, world, rank, local, cpu_baseline):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(K):
-        layer.forward(x, expert_events=ev_exp[i], load_group=lg)
+        layer.forward(x, expert_events=ev_exp[i], load_group=lg, gated=gated)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -526,7 +527,7 @@ def measure_ours(args, shape, world, rank, local, cpu_baseline):
             stream.wait_event(h2d_done[b])
             if used[b]:
                 stream.wait_event(d2h_done[b])  # step i-2's output has been read back
-            layer.forward(x_dev[b], out=out_dev[b], load_group=lg)
+            layer.forward(x_dev[b], out=out_dev[b], load_group=lg, gated=gated)
             comp_done[b].record(stream)
             used[b] = True
             d2h_s.wait_event(comp_done[b])
@@ -591,6 +592,8 @@ def measure_ours(args, shape, world, rank, local, cpu_baseline):
         "config": {"workload": describe(shape), "global_batch": world * shape.T,
                    "dispatch": "gather rows inside the gate/up GEMM" if gather
                                else "permute kernel before the expert GEMMs",
+                   "combine": "gates folded into the down projection; combine adds rows"
+                              if gated else "combine multiplies rows by their gates",
                    "parallelism": f"data-parallel replicas x{world}, one all-reduce of the "
                                   f"per-expert loads per step" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: every step streams all expert weights "
@@ -601,7 +604,7 @@ def measure_ours(args, shape, world, rank, local, cpu_baseline):
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": out_host[0].numel() * out_host[0].element_size(),
                 "copies": "pipelined on two copy streams (double-buffered)"},
-        "gpu_launches": launches_per_step(shape, gather) * K,
+        "gpu_launches": (launches_per_step(shape, gather) + (1 if gated else 0)) * K,
         "clocks": clk,
     }
     if shape.bias_steps:
@@ -776,6 +779,9 @@ def main():
     ap.add_argument("--dispatch", choices=["permute", "gather"], default="permute",
                     help="bf16 kind: permute x into per-expert rows before the expert GEMMs, "
                          "or gather the rows inside the gate/up GEMM")
+    ap.add_argument("--gated", action="store_true",
+                    help="fold the gate multiply into the down projection "
+                         "(moe_experts_grouped_gated); the combine then only adds rows")
     ap.add_argument("--train", action="store_true",
                     help="time a training step (forward + backward; bf16 kind)")
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",

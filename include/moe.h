@@ -223,11 +223,41 @@ moe_status_t moe_experts_grouped_gather(const moe_cfg_t* cfg, const void* x,
                                         void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_experts_grouped_gated - moe_experts_grouped with the gate multiply of
+ * the DeepSeekMoE paragraph's weighted sum folded into the down projection:
+ *   y_perm[r] = g_{t,k} * FFN_e(u_t)   for the copy (t, k) that row r holds,
+ * the gate applied to the fp32 sum before the one rounding to the output
+ * type.  moe_combine(..., topk_w = NULL, ...) then only adds the rows.
+ *
+ *   row_of_slot, topk_w  [T, K] from moe_route (required)
+ *   everything else as in moe_experts_grouped; y_shared is not gated
+ *
+ * All kinds.  The gates of the permuted rows are scattered into the
+ * workspace first (one small kernel): moe_workspace_bytes covers them.  A
+ * row index outside [0, T*K) sets the error word (MOE_ERR_DEVICE) and is
+ * skipped.  The backward pass needs the ungated y_perm (dL/dg = dL/dy . y):
+ * train with moe_experts_grouped_train and the gated moe_combine.
+ */
+moe_status_t moe_experts_grouped_gated(const moe_cfg_t* cfg, const void* x_perm,
+                                       const float* x_perm_scales, const void* x,
+                                       const float* x_scales, const int32_t* offsets,
+                                       const void* w13, const float* w13_scales,
+                                       const void* w2, const float* w2_scales,
+                                       const void* ws13, const float* ws13_scales,
+                                       const void* ws2, const float* ws2_scales,
+                                       const int32_t* row_of_slot, const float* topk_w,
+                                       void* y_perm, void* y_shared, void* ws,
+                                       size_t ws_bytes, void* stream);
+
+/*
  * moe_combine - gate-weighted un-permute:
  *   out[t] = y_shared[t] + sum_{k < K} topk_w[t, k] * y_perm[row_of_slot[t, k]]
  * summed in fp32 in exactly that order (DeepSeekMoE paragraph).
  *
  *   y_perm [T*K, d], y_shared [T, d] (nullable): fp32 (FP32 kind) or bf16
+ *   topk_w [T, K] fp32, or NULL when y_perm already holds the gated rows
+ *          of moe_experts_grouped_gated (then out[t] = y_shared[t] +
+ *          sum_k y_perm[row_of_slot[t, k]], same order)
  *   out    [T, d] fp32 (FP32 kind) or bf16
  */
 moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y_perm,

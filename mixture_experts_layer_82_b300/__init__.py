@@ -42,7 +42,7 @@ EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_byt
             "moe_route_static_scratch", "moe_experts_grouped_gather", "moe_balance_stat",
             "moe_selftest_wait", "moe_backward_workspace_bytes", "moe_combine_backward",
             "moe_experts_backward_input", "moe_experts_backward_weights", "moe_route_backward",
-            "moe_experts_grouped_train")
+            "moe_experts_grouped_train", "moe_experts_grouped_gated")
 
 
 class MoeCfg(ctypes.Structure):
@@ -77,6 +77,8 @@ _lib.moe_permute.restype = ctypes.c_int
 _lib.moe_permute.argtypes = [_CFG] + [_P] * 6 + [_P]
 _lib.moe_experts_grouped.restype = ctypes.c_int
 _lib.moe_experts_grouped.argtypes = [_CFG] + [_P] * 15 + [_P, ctypes.c_size_t, _P]
+_lib.moe_experts_grouped_gated.restype = ctypes.c_int
+_lib.moe_experts_grouped_gated.argtypes = [_CFG] + [_P] * 17 + [_P, ctypes.c_size_t, _P]
 _lib.moe_experts_grouped_gather.restype = ctypes.c_int
 _lib.moe_experts_grouped_gather.argtypes = [_CFG] + [_P] * 14 + [_P, ctypes.c_size_t, _P]
 _lib.moe_balance_stat.restype = ctypes.c_int
@@ -249,6 +251,31 @@ def moe_experts_grouped(cfg, x_perm, x, offsets, w13, w2, ws13, ws2, y_perm, y_s
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+
+def moe_experts_grouped_gated(cfg, x_perm, x, offsets, w13, w2, ws13, ws2, row_of_slot, topk_w,
+                              y_perm, y_shared, ws,
+                              x_perm_scales=None, x_scales=None, w13_scales=None, w2_scales=None,
+                              ws13_scales=None, ws2_scales=None, stream=None):
+    """moe_experts_grouped whose routed output rows carry their gates
+    (y_perm[r] = g * FFN(u) for the copy r holds); combine them with
+    ``moe_combine(..., topk_w=None, ...)``."""
+    _check("moe_experts_grouped_gated", _lib.moe_experts_grouped_gated(
+        _cfg(cfg), _ptr(x_perm, "x_perm", _X + _F8),
+        _ptr(x_perm_scales, "x_perm_scales", torch.float32, allow_none=True),
+        _ptr(x, "x", _X + _F8, allow_none=True),
+        _ptr(x_scales, "x_scales", torch.float32, allow_none=True),
+        _ptr(offsets, "offsets", torch.int32), _ptr(w13, "w13", _X + _F8),
+        _ptr(w13_scales, "w13_scales", torch.float32, allow_none=True),
+        _ptr(w2, "w2", _X + _F8), _ptr(w2_scales, "w2_scales", torch.float32, allow_none=True),
+        _ptr(ws13, "ws13", _X + _F8, allow_none=True),
+        _ptr(ws13_scales, "ws13_scales", torch.float32, allow_none=True),
+        _ptr(ws2, "ws2", _X + _F8, allow_none=True),
+        _ptr(ws2_scales, "ws2_scales", torch.float32, allow_none=True),
+        _ptr(row_of_slot, "row_of_slot", torch.int32), _ptr(topk_w, "topk_w", torch.float32),
+        _ptr(y_perm, "y_perm", _X), _ptr(y_shared, "y_shared", _X, allow_none=True),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def moe_experts_grouped_gather(cfg, x, token_of_row, offsets, w13, w2, ws13, ws2, y_perm,
                                y_shared, ws, x_scales=None, w13_scales=None, w2_scales=None,
                                ws13_scales=None, ws2_scales=None, stream=None):
@@ -281,9 +308,11 @@ def moe_balance_stat(cfg, affinity, topk_idx, seq_len, f_out, p_out, loss_out, w
 
 
 def moe_combine(cfg, y_perm, y_shared, row_of_slot, topk_w, out, stream=None):
+    """``topk_w=None``: y_perm holds the gated rows of moe_experts_grouped_gated."""
     _check("moe_combine", _lib.moe_combine(
         _cfg(cfg), _ptr(y_perm, "y_perm", _X), _ptr(y_shared, "y_shared", _X, allow_none=True),
-        _ptr(row_of_slot, "row_of_slot", torch.int32), _ptr(topk_w, "topk_w", torch.float32),
+        _ptr(row_of_slot, "row_of_slot", torch.int32),
+        _ptr(topk_w, "topk_w", torch.float32, allow_none=True),
         _ptr(out, "out", _X), _stream(stream)))
 
 

@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(256) simt_down_kernel(
     const float* __restrict__ h_routed, const float* __restrict__ h_shared,
     const int32_t* __restrict__ offsets, const float* __restrict__ w2, const float* __restrict__ ws2,
     float* __restrict__ y_perm, float* __restrict__ y_shared, int E, int T, int n_rows, int d, int inter,
-    int n_shared) {
+    int n_shared, const float* __restrict__ gate_of_row) {
   SimtGroup g;
   if (!simt_find_group(offsets, E, T, n_rows, n_shared > 0, blockIdx.y, g)) return;
   const int kdim = g.cls == 0 ? inter : n_shared * inter;
@@ -158,10 +158,12 @@ __global__ void __launch_bounds__(256) simt_down_kernel(
   for (int i = 0; i < 4; ++i) {
     const int m = m0 + ty * 4 + i;
     if (m >= g.rows) continue;
+    // the routed rows' gate, folded in before the store
+    const float gm = g.cls == 0 && gate_of_row != nullptr ? gate_of_row[g.row0 + m] : 1.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tx * 4 + j;
-      if (n < d) Y[static_cast<size_t>(m) * d + n] = acc[i][j];
+      if (n < d) Y[static_cast<size_t>(m) * d + n] = acc[i][j] * gm;
     }
   }
 }
@@ -184,7 +186,8 @@ cudaError_t launch_experts_fp32(const ExpertsArgs& a, cudaStream_t st) {
   simt_down_kernel<<<dim3(ceil_div(c.d, kSBN), m_tiles), 256, 0, st>>>(
       h_routed, h_shared, a.offsets, static_cast<const float*>(a.w2),
       static_cast<const float*>(a.ws2), static_cast<float*>(a.y_perm),
-      static_cast<float*>(a.y_shared), c.E, c.T, static_cast<int>(tk), c.d, c.inter, c.n_shared);
+      static_cast<float*>(a.y_shared), c.E, c.T, static_cast<int>(tk), c.d, c.inter, c.n_shared,
+      a.gate_of_row);
   return cudaGetLastError();
 }
 

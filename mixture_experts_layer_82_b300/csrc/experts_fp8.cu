@@ -80,6 +80,7 @@ struct ClassDesc {
   const float* w_scales;  // block scales of the class's weight matrices
   int n_out;              // output columns (row stride of out)
   int k_dim;              // reduction length
+  const float* gate;      // down, optional: every output row is multiplied by gate[row]
 };
 
 struct Params {
@@ -551,13 +552,16 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
       } else {
         const int n_base = tl.nt * BN + hf * 128;
         if (valid) {
+          // the routed rows' gate, folded in before the one rounding to bf16
+          const float gm = cd.gate != nullptr ? cd.gate[grow] : 1.f;
           __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(cd.out) + grow * cd.n_out + n_base;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             if (n_base + c * 16 < cd.n_out) {
               uint32_t w[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(acc[c * 16 + 2 * i], acc[c * 16 + 2 * i + 1]);
+              for (int i = 0; i < 8; ++i)
+                w[i] = pack_bf16x2(acc[c * 16 + 2 * i] * gm, acc[c * 16 + 2 * i + 1] * gm);
               if (p.out32) {
                 st_global_32B(orow + c * 16, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
               } else {
@@ -649,7 +653,7 @@ cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t st) {
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   dn.out32 = al32(a.y_perm) && (!has_shared || al32(a.y_shared)) ? 1 : 0;
-  dn.cls[0] = ClassDesc{a.y_perm, nullptr, hs_routed, a.w2_scales, c.d, I};
+  dn.cls[0] = ClassDesc{a.y_perm, nullptr, hs_routed, a.w2_scales, c.d, I, a.gate_of_row};
   dn.cls[1] = ClassDesc{has_shared ? a.y_shared : a.y_perm, nullptr,
                         has_shared ? hs_shared : hs_routed,
                         has_shared ? a.ws2_scales : a.w2_scales, c.d, Ns > 0 ? Ns * I : I};

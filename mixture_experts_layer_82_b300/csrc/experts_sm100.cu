@@ -74,6 +74,7 @@ struct ClassDesc {
   int k_dim;           // reduction length
   __nv_bfloat16* ab;   // gate/up, optional: [a | b] of every expert kept for the backward
   int ld_ab;           // its row stride (2I per expert of the class)
+  const float* gate;   // down, optional: every output row is multiplied by gate[row]
 };
 
 struct Params {
@@ -496,6 +497,8 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
           }
         }
       } else {
+        // the routed rows' gate, folded in before the one rounding to bf16
+        const float gm = cd.gate != nullptr && valid ? cd.gate[tl.row0 + m] : 1.f;
 #pragma unroll 1
         for (int c = 0; c < BN / 16; ++c) {
           float v[16];
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
           tmem_ld_wait();
           uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(v[2 * i] * gm, v[2 * i + 1] * gm);
           if (valid && n_base + c * 16 < cd.n_out) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -529,13 +532,22 @@ __global__ void __launch_bounds__(GATHER ? THREADS_GATHER : THREADS, 1)
 }  // namespace bf16gemm
 
 // ------------------------------------------------------------------- host
-size_t experts_scratch_bytes(const moe_cfg_t& c) {
+// h (and, FP8, its scales), then the gate of every permuted row.
+static size_t experts_h_bytes(const moe_cfg_t& c) {
   const size_t tk = static_cast<size_t>(c.T) * c.K;
   const size_t hr = tk * c.inter, hs = static_cast<size_t>(c.T) * c.n_shared * c.inter;
   if (c.dtype == MOE_DTYPE_FP32) return align_up((hr + hs) * 4, 256);
   if (c.dtype == MOE_DTYPE_BF16) return align_up((hr + hs) * 2, 256);
   // FP8: E4M3 codes plus one fp32 scale per 128 values
   return align_up(hr + hs, 256) + align_up((hr + hs) / 128 * 4, 256);
+}
+
+size_t experts_scratch_bytes(const moe_cfg_t& c) {
+  return experts_h_bytes(c) + align_up(static_cast<size_t>(c.T) * c.K * 4, 256);
+}
+
+float* experts_gate_rows(const moe_cfg_t& c, void* ws) {
+  return reinterpret_cast<float*>(static_cast<char*>(ws) + experts_h_bytes(c));
 }
 
 void experts_scratch_carve(const moe_cfg_t& c, void* ws, void** h, float** h_scales) {
@@ -666,7 +678,8 @@ cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t st) {
     dn.b_half[1] = dn.b_half[0];
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  dn.cls[0] = ClassDesc{static_cast<__nv_bfloat16*>(a.y_perm), c.d, c.d, I};
+  dn.cls[0] = ClassDesc{static_cast<__nv_bfloat16*>(a.y_perm), c.d, c.d, I, nullptr, 0,
+                        a.gate_of_row};
   dn.cls[1] = ClassDesc{static_cast<__nv_bfloat16*>(a.y_shared), c.d, c.d, Ns * I};
   return launch_bf16_gemm<DOWN, false>(dn, st);
 }

@@ -54,6 +54,9 @@ cudaError_t launch_quantize_act_fp8(const void* x_bf16, int rows, int cols, void
 cudaError_t launch_permute_fp8(const moe_cfg_t& c, const void* x_q, const float* x_scales,
                                const int32_t* token_of_row, void* x_perm, float* x_perm_scales,
                                cudaStream_t s);
+// gate_of_row[row_of_slot[i]] = topk_w[i] for every (token, slot) i.
+cudaError_t launch_gate_rows(const moe_cfg_t& c, const int32_t* row_of_slot, const float* topk_w,
+                             float* gate_of_row, cudaStream_t s);
 cudaError_t launch_combine(const moe_cfg_t& c, const void* y_perm, const void* y_shared,
                            const int32_t* row_of_slot, const float* topk_w, void* out,
                            cudaStream_t s);
@@ -83,10 +86,13 @@ struct ExpertsArgs {
   float* h_scales;    // FP8: [T*K, I/128] then [T, Ns*I/128]
   __nv_bfloat16* ab;         // bf16 training forward, optional: [a | b] rows kept for
   __nv_bfloat16* ab_shared;  // the backward ([T*K, 2I] and [T, Ns*2I])
+  const float* gate_of_row;  // optional [T*K]: the down projection writes gate * y
 };
 
 size_t experts_scratch_bytes(const moe_cfg_t& c);
 void experts_scratch_carve(const moe_cfg_t& c, void* ws, void** h, float** h_scales);
+// The gate of every permuted row ([T*K] fp32) in the experts' scratch.
+float* experts_gate_rows(const moe_cfg_t& c, void* ws);
 
 cudaError_t launch_experts_fp32(const ExpertsArgs& a, cudaStream_t s);
 cudaError_t launch_experts_bf16(const ExpertsArgs& a, cudaStream_t s);

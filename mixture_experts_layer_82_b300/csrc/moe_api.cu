@@ -149,13 +149,18 @@ moe_status_t moe_permute(const moe_cfg_t* cfg, const void* x, const int32_t* tok
   return from_cuda(e);
 }
 
-moe_status_t moe_experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
-                                 const float* x_perm_scales, const void* x, const float* x_scales,
-                                 const int32_t* offsets, const void* w13, const float* w13_scales,
-                                 const void* w2, const float* w2_scales, const void* ws13,
-                                 const float* ws13_scales, const void* ws2, const float* ws2_scales,
-                                 void* y_perm, void* y_shared, void* ws, size_t ws_bytes,
-                                 void* stream) {
+}  // extern "C"
+
+// moe_experts_grouped, and with row_of_slot / topk_w given, its gated form.
+static moe_status_t experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
+                                    const float* x_perm_scales, const void* x,
+                                    const float* x_scales, const int32_t* offsets, const void* w13,
+                                    const float* w13_scales, const void* w2,
+                                    const float* w2_scales, const void* ws13,
+                                    const float* ws13_scales, const void* ws2,
+                                    const float* ws2_scales, const int32_t* row_of_slot,
+                                    const float* topk_w, void* y_perm, void* y_shared, void* ws,
+                                    size_t ws_bytes, void* stream) {
   moe_status_t st = moe_check_cfg(cfg);
   if (st != MOE_OK) return st;
   const moe_cfg_t& c = *cfg;
@@ -170,7 +175,8 @@ moe_status_t moe_experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
                                   ws2_scales == nullptr))))
     return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x_perm, x_perm_scales, x, x_scales, offsets, w13, w13_scales, w2,
-                        w2_scales, ws13, ws13_scales, ws2, ws2_scales, y_perm, y_shared, ws};
+                        w2_scales, ws13, ws13_scales, ws2, ws2_scales, y_perm, y_shared, ws,
+                        row_of_slot, topk_w};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
   if (ws_bytes < experts_scratch_bytes(c)) return MOE_ERR_WORKSPACE;
@@ -184,12 +190,47 @@ moe_status_t moe_experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
   experts_scratch_carve(c, ws, &a.h, &a.h_scales);
   cudaStream_t s = as_stream(stream);
   cudaError_t e;
+  if (row_of_slot != nullptr) {
+    float* gate_rows = experts_gate_rows(c, ws);
+    e = launch_gate_rows(c, row_of_slot, topk_w, gate_rows, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    a.gate_of_row = gate_rows;
+  }
   switch (c.dtype) {
     case MOE_DTYPE_FP32: e = launch_experts_fp32(a, s); break;
     case MOE_DTYPE_BF16: e = launch_experts_bf16(a, s); break;
     default: e = launch_experts_fp8(a, s); break;
   }
   return from_cuda(e);
+}
+
+extern "C" {
+
+moe_status_t moe_experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
+                                 const float* x_perm_scales, const void* x, const float* x_scales,
+                                 const int32_t* offsets, const void* w13, const float* w13_scales,
+                                 const void* w2, const float* w2_scales, const void* ws13,
+                                 const float* ws13_scales, const void* ws2, const float* ws2_scales,
+                                 void* y_perm, void* y_shared, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  return experts_grouped(cfg, x_perm, x_perm_scales, x, x_scales, offsets, w13, w13_scales, w2,
+                         w2_scales, ws13, ws13_scales, ws2, ws2_scales, nullptr, nullptr, y_perm,
+                         y_shared, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_experts_grouped_gated(const moe_cfg_t* cfg, const void* x_perm,
+                                       const float* x_perm_scales, const void* x,
+                                       const float* x_scales, const int32_t* offsets,
+                                       const void* w13, const float* w13_scales, const void* w2,
+                                       const float* w2_scales, const void* ws13,
+                                       const float* ws13_scales, const void* ws2,
+                                       const float* ws2_scales, const int32_t* row_of_slot,
+                                       const float* topk_w, void* y_perm, void* y_shared,
+                                       void* ws, size_t ws_bytes, void* stream) {
+  if (row_of_slot == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+  return experts_grouped(cfg, x_perm, x_perm_scales, x, x_scales, offsets, w13, w13_scales, w2,
+                         w2_scales, ws13, ws13_scales, ws2, ws2_scales, row_of_slot, topk_w,
+                         y_perm, y_shared, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_experts_grouped_gather(const moe_cfg_t* cfg, const void* x,
@@ -230,8 +271,8 @@ moe_status_t moe_combine(const moe_cfg_t* cfg, const void* y_perm, const void* y
   moe_status_t st = moe_check_cfg(cfg);
   if (st != MOE_OK) return st;
   const moe_cfg_t& c = *cfg;
-  if (y_perm == nullptr || row_of_slot == nullptr || topk_w == nullptr || out == nullptr)
-    return MOE_ERR_INVALID_ARG;
+  // topk_w NULL: the rows already carry their gates (moe_experts_grouped_gated)
+  if (y_perm == nullptr || row_of_slot == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {y_perm, y_shared, row_of_slot, topk_w, out};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;

@@ -243,7 +243,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) combine_kernel(
     float my_g = 0.f;
     if (lane < K) {
       my_row = row_of_slot[t * K + lane];
-      my_g = topk_w[t * K + lane];
+      // no gates: the rows already hold gate * y (a plain ordered sum)
+      my_g = topk_w != nullptr ? topk_w[t * K + lane] : 1.f;
       if (my_row < 0 || my_row >= n_rows) { raise_error(kErrIndex); my_row = 0; }
     }
     float acc[kCombineVecs][n];
@@ -277,6 +278,27 @@ __global__ void __launch_bounds__(kRowWarps * 32) combine_kernel(
       if (c < d) V::store(out + t * d + c, acc[v]);
     }
   }
+}
+
+// Gate of every permuted row: the row of (token t, slot k) takes g[t, k]
+// (the DeepSeekMoE paragraph's gate of that expert for that token).
+__global__ void gate_rows_kernel(const int32_t* __restrict__ row_of_slot,
+                                 const float* __restrict__ topk_w, float* __restrict__ gate_of_row,
+                                 int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = row_of_slot[i];
+    if (row < 0 || row >= n) { raise_error(kErrIndex); continue; }
+    gate_of_row[row] = topk_w[i];
+  }
+}
+
+cudaError_t launch_gate_rows(const moe_cfg_t& c, const int32_t* row_of_slot, const float* topk_w,
+                             float* gate_of_row, cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(c.T) * c.K;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 148 * 8));
+  gate_rows_kernel<<<blocks, 256, 0, st>>>(row_of_slot, topk_w, gate_of_row, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const moe_cfg_t& c, const void* y_perm, const void* y_shared,

@@ -9,6 +9,7 @@ import torch
 
 from .replicas import global_cfg, global_load
 from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_experts_grouped_gather,
+               moe_experts_grouped_gated,
                moe_combine, moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes,
                moe_backward_workspace_bytes, moe_combine_backward, moe_experts_backward_input,
                moe_experts_backward_weights, moe_route_backward, moe_experts_grouped_train)
@@ -71,7 +72,8 @@ class MoELayer:
         self.ws = torch.empty(moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
 
     def forward(self, x, stream=None, update_bias=True, affinity_out=None, affinity_in=None,
-                expert_events=None, gather=None, out=None, keep=False, load_group=None):
+                expert_events=None, gather=None, out=None, keep=False, load_group=None,
+                gated=False):
         """One forward step on ``x`` [T, d]; returns the layer output, written
         to ``out`` when given (else to the layer's own buffer).
         ``expert_events`` (a pair of torch.cuda.Event) are recorded on
@@ -82,11 +84,16 @@ class MoELayer:
         next ``backward`` instead of having it recompute them.
         ``load_group``: a torch.distributed group of data-parallel replicas;
         the bias update then uses the whole batch's per-expert loads (one
-        all-reduce of ``counts``, which afterwards hold the global loads)."""
+        all-reduce of ``counts``, which afterwards hold the global loads).
+        ``gated`` (permuting forward without ``keep``): the down projection
+        multiplies each routed row by its gate (moe_experts_grouped_gated)
+        and the combine only adds rows; ``y_perm`` then holds the gated
+        rows."""
         c = self.cfg
         out = self.out if out is None else out
         gather = self.gather if gather is None else gather
         keep = keep and c.dtype == "bf16" and not gather
+        gated = gated and not gather and not keep
         if keep and not hasattr(self, "bws"):
             self._grad_buffers()
         self._ab_kept = False
@@ -110,6 +117,14 @@ class MoELayer:
                                           self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
                                           self.bws, stream=stream)
                 self._ab_kept = True
+            elif gated:
+                moe_experts_grouped_gated(c, self.x_perm, shared_in, self.offsets, self.w13,
+                                          self.w2, self.ws13, self.ws2, self.row_of_slot,
+                                          self.topk_w, self.y_perm, self.y_shared, self.ws,
+                                          x_perm_scales=self.x_perm_s, x_scales=self.x_q_s,
+                                          w13_scales=self.w13_s, w2_scales=self.w2_s,
+                                          ws13_scales=self.ws13_s, ws2_scales=self.ws2_s,
+                                          stream=stream)
             else:
                 moe_experts_grouped(c, self.x_perm, shared_in, self.offsets, self.w13, self.w2,
                                     self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
@@ -118,8 +133,8 @@ class MoELayer:
                                     ws13_scales=self.ws13_s, ws2_scales=self.ws2_s, stream=stream)
         if expert_events is not None:
             expert_events[1].record(stream)
-        moe_combine(c, self.y_perm, self.y_shared, self.row_of_slot, self.topk_w, out,
-                    stream=stream)
+        moe_combine(c, self.y_perm, self.y_shared, self.row_of_slot,
+                    None if gated else self.topk_w, out, stream=stream)
         if update_bias:
             if load_group is not None:
                 world = global_load(self.counts, load_group, stream=stream)

@@ -23,6 +23,7 @@ from .moe_oracle import (  # noqa: F401
     silu,
     swiglu_ffn,
     combine,
+    gate_of_row,
     bias_update,
     moe_layer_forward,
     moe_layer_tokens,

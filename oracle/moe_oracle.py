@@ -223,6 +223,18 @@ def combine(y_shared, y_perm, row_of_slot, gates):
     return out
 
 
+def gate_of_row(row_of_slot, gates):
+    """Gate of every permuted row: the row holding token t's copy for slot j
+    carries g[t, j] (the weight of that expert's output in the DeepSeekMoE
+    paragraph's sum).  With y_perm's rows multiplied by it, the combine is a
+    plain sum: combine(y_shared, gate_of_row * y_perm, rows, 1) equals
+    combine(y_shared, y_perm, rows, g)."""
+    ros = np.asarray(row_of_slot)
+    g = np.zeros(ros.size, dtype=np.float64)
+    g[ros.reshape(-1)] = np.asarray(gates, dtype=np.float64).reshape(-1)
+    return g
+
+
 # --------------------------------------------------------------------------
 # Auxiliary-loss-free bias update
 # --------------------------------------------------------------------------

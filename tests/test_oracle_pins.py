@@ -549,3 +549,26 @@ def test_load_spread_hand_example():
     b = bench.load_stats([0, 2, 4, 6], T=4, K=3)
     assert b["max_over_mean"] == 2.0 and abs(b["cv"] - np.sqrt(5.0) / 3.0) < 1e-15
     assert (b["min"], b["max"], b["empty_experts"]) == (0, 6, 1)
+
+
+def test_gate_of_row_makes_the_combine_a_plain_sum():
+    """Scaling each permuted row by its slot's gate and then adding rows with
+    unit weights is the gate-weighted combine (DeepSeekMoE paragraph), and
+    every row receives exactly the gate of the (token, slot) it holds."""
+    rng = np.random.default_rng(21)
+    T, E, K, d = 37, 12, 3, 16
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    _, _, ros, tor = oracle.segment_layout(idx, E)
+    g = rng.random((T, K))
+    y = rng.standard_normal((T * K, d))
+    ys = rng.standard_normal((T, d))
+    gr = oracle.gate_of_row(ros, g)
+    assert gr.shape == (T * K,)
+    for t in range(T):
+        for j in range(K):
+            assert gr[ros[t, j]] == g[t, j]
+    np.testing.assert_allclose(oracle.combine(ys, gr[:, None] * y, ros, np.ones((T, K))),
+                               oracle.combine(ys, y, ros, g), rtol=1e-14, atol=1e-14)
+    # a wrong pairing (gates of the next slot) is visible
+    bad = oracle.gate_of_row(ros, np.roll(g, 1, axis=1))
+    assert np.max(np.abs(bad - gr)) > 1e-3
