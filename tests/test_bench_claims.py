@@ -9,11 +9,14 @@ import sys
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
+import pytest  # noqa: E402
+
 import bench  # noqa: E402
 from moe_synth import CONFIGS  # noqa: E402
 
 
 def _kernel_rows(name):
+    """(kernel, launches) rows of a launch list that counts launches per kernel."""
     rows = []
     with open(os.path.join(ROOT, "profiles", name)) as f:
         for line in f:
@@ -23,11 +26,24 @@ def _kernel_rows(name):
     return rows
 
 
-def test_forward_launches_match_the_launch_list():
-    rows = _kernel_rows("launches_v3_bf16.md")
-    # every kernel of the step appears once per step, 11 steps in the list
-    assert all(n == 11 for _, n in rows)
-    assert bench.launches_per_step(CONFIGS["v3_bf16"]) == len(rows)
+def _step_rows(name):
+    """Kernel rows of a launch list of one captured step (kernel | grid | ...)."""
+    rows = []
+    with open(os.path.join(ROOT, "profiles", name)) as f:
+        for line in f:
+            m = re.match(r"\| ([^|]+) \| (\([0-9,]+\)) \|", line)
+            if m:
+                rows.append(m.group(1).strip())
+    return rows
+
+
+@pytest.mark.parametrize("workload", ["v3_bf16", "v3_fp8", "v3_decode"])
+def test_forward_launches_match_the_launch_list(workload):
+    rows = _step_rows(f"launches_{workload}.md")
+    # one row per launch of the captured step
+    assert bench.launches_per_step(CONFIGS[workload]) == len(rows)
+    assert sum("experts_" in r for r in rows) == 2
+    assert sum("combine" in r for r in rows) == 1
 
 
 def test_training_launches_match_the_launch_list():
