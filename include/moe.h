@@ -335,11 +335,15 @@ moe_status_t moe_balance_stat(const moe_cfg_t* cfg, const float* affinity,
  * order: results are deterministic.
  */
 
-/* Scratch of the backward calls: align256((T*K + T*N_s) * 3I * 2) bytes of
- * expert intermediates ([a | b] then [da | db], and h; they must survive
- * from moe_experts_backward_input to moe_experts_backward_weights) plus
- * align256(T*K*4) bytes for moe_route_backward.  0 for a configuration the
- * backward does not support. */
+/* Scratch of the backward calls: the expert part, then align256(T*K*4)
+ * bytes for moe_route_backward.  BF16 kind: align256((T*K + T*N_s) * 3I * 2)
+ * bytes of expert intermediates ([a | b] then [da | db], and h; they must
+ * survive from moe_experts_backward_input to moe_experts_backward_weights).
+ * FP8 kind (N_s <= 1): the buffers of moe_experts_backward_input_fp8 for
+ * T*K + T rows (q(dy) codes and scales, [a | b] and dh in bf16, q([da | db])
+ * codes and scales).  0 for a configuration the backward does not support.
+ * moe_combine_backward and moe_route_backward take both kinds (their data
+ * are bf16 in both); the other backward calls name their kind. */
 size_t moe_backward_workspace_bytes(const moe_cfg_t* cfg);
 
 /*
@@ -433,6 +437,52 @@ moe_status_t moe_route_backward(const moe_cfg_t* cfg, const void* x, const float
                                 const void* dx_perm, const void* dx_shared, float* dlogit,
                                 void* dx, float* drouter_w, void* ws, size_t ws_bytes,
                                 void* stream);
+
+/*
+ * moe_transpose_weights_fp8 - offline utility for the FP8 backward:
+ * transposes `n_mats` E4M3 matrices [rows, cols] (rows, cols % 128 == 0) to
+ * [cols, rows], and their 128 x 128 block scales [n, rows/128, cols/128] to
+ * [n, cols/128, rows/128].  The blocks are the same blocks, so a transposed
+ * copy quantises nothing again: W2 [E, d, I] gives W2^T [E, I, d] and W13
+ * [E, 2I, d] gives W13^T [E, d, 2I] for moe_experts_backward_input_fp8.
+ */
+moe_status_t moe_transpose_weights_fp8(const void* w_q, const float* w_scales,
+                                       int32_t n_mats, int32_t rows, int32_t cols,
+                                       void* wt_q, float* wt_scales, void* stream);
+
+/*
+ * moe_experts_backward_input_fp8 - Dgrad of every expert FFN in FP8 E4M3
+ * (mixed precision framework paragraph, Figure 6: Dgrad in FP8 with fp32
+ * accumulation; fine-grained quantisation paragraph: 1 x 128 activation
+ * tiles, 128 x 128 weight blocks).  The gradients are tiled along the
+ * contraction of their GEMM, so that each tile's scale factors out:
+ *   [a | b] = u W13^T   recomputed from the forward's E4M3 codes of u
+ *   dh = q(dy) W2       dy (bf16) in 1 x 128 tiles along d
+ *   da = dh b silu'(a), db = dh silu(a)   in fp32
+ *   du = q([da | db]) W13   [da | db] in 1 x 128 tiles along 2I
+ * with scale fl32(amax / 448) per tile and fp32 promotion of every
+ * 128-deep partial sum, as in the FP8 forward.
+ *   x_perm, x_perm_scales    the forward's E4M3 rows and scales (moe_permute)
+ *   x_q, x_q_scales          the forward's E4M3 token rows (shared expert)
+ *   offsets [E + 1]          from moe_route
+ *   w13, w13_scales          [E, 2I, d] forward codes and block scales
+ *   w13t, w13t_scales        [E, d, 2I] their transpose (moe_transpose_weights_fp8)
+ *   w2t, w2t_scales          [E, I, d]  the transpose of the forward's W2
+ *   ws13.., ws13t.., ws2t..  the same for the shared expert (NULL if N_s = 0)
+ *   dy_perm [T*K, d] bf16    from moe_combine_backward
+ *   dout    [T, d] bf16      dL/dy of the layer (the shared expert's dy)
+ *   dx_perm [T*K, d] bf16 out, dx_shared [T, d] bf16 out (NULL if N_s = 0)
+ *   ws, ws_bytes             at least moe_backward_workspace_bytes(cfg)
+ * FP8 kind with at most one shared expert (MOE_ERR_SHAPE otherwise).  The
+ * weight gradients of the FP8 kind are not computed by this library.
+ */
+moe_status_t moe_experts_backward_input_fp8(
+    const moe_cfg_t* cfg, const void* x_perm, const float* x_perm_scales, const void* x_q,
+    const float* x_q_scales, const int32_t* offsets, const void* w13, const float* w13_scales,
+    const void* w13t, const float* w13t_scales, const void* w2t, const float* w2t_scales,
+    const void* ws13, const float* ws13_scales, const void* ws13t, const float* ws13t_scales,
+    const void* ws2t, const float* ws2t_scales, const void* dy_perm, const void* dout,
+    void* dx_perm, void* dx_shared, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * moe_quantize_weights_fp8 - offline utility: quantise `n_mats` bf16

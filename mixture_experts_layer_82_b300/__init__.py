@@ -42,7 +42,8 @@ EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_byt
             "moe_route_static_scratch", "moe_experts_grouped_gather", "moe_balance_stat",
             "moe_selftest_wait", "moe_backward_workspace_bytes", "moe_combine_backward",
             "moe_experts_backward_input", "moe_experts_backward_weights", "moe_route_backward",
-            "moe_experts_grouped_train", "moe_experts_grouped_gated")
+            "moe_experts_grouped_train", "moe_experts_grouped_gated", "moe_transpose_weights_fp8",
+            "moe_experts_backward_input_fp8")
 
 
 class MoeCfg(ctypes.Structure):
@@ -108,6 +109,11 @@ _lib.moe_experts_grouped_train.argtypes = ([_CFG] + [_P] * 10 + [ctypes.c_size_t
                                            [_P, ctypes.c_size_t, _P])
 _lib.moe_experts_backward_weights.argtypes = [_CFG] + [_P] * 9 + [_P, ctypes.c_size_t, _P]
 _lib.moe_route_backward.argtypes = [_CFG] + [_P] * 13 + [_P, ctypes.c_size_t, _P]
+_lib.moe_transpose_weights_fp8.restype = ctypes.c_int
+_lib.moe_transpose_weights_fp8.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                           _P, _P, _P]
+_lib.moe_experts_backward_input_fp8.restype = ctypes.c_int
+_lib.moe_experts_backward_input_fp8.argtypes = [_CFG] + [_P] * 21 + [_P, ctypes.c_size_t, _P]
 
 
 def library():
@@ -387,6 +393,37 @@ def moe_route_backward(cfg, x, router_w, affinity, topk_idx, dgate, row_of_slot,
         _ptr(dx_perm, "dx_perm", _BF), _ptr(dx_shared, "dx_shared", _BF, allow_none=True),
         _ptr(dlogit, "dlogit", torch.float32), _ptr(dx, "dx", _BF),
         _ptr(drouter_w, "drouter_w", torch.float32),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_transpose_weights_fp8(q, scales, qt, scales_t, stream=None):
+    """E4M3 matrices [n, rows, cols] and their 128 x 128 block scales,
+    transposed into ``qt`` [n, cols, rows] and ``scales_t``."""
+    n, rows, cols = q.shape
+    _check("moe_transpose_weights_fp8", _lib.moe_transpose_weights_fp8(
+        _ptr(q, "q", _F8), _ptr(scales, "scales", torch.float32), n, rows, cols,
+        _ptr(qt, "qt", _F8), _ptr(scales_t, "scales_t", torch.float32), _stream(stream)))
+
+
+def moe_experts_backward_input_fp8(cfg, x_perm, x_perm_scales, x_q, x_q_scales, offsets, w13,
+                                   w13_scales, w13t, w13t_scales, w2t, w2t_scales, ws13,
+                                   ws13_scales, ws13t, ws13t_scales, ws2t, ws2t_scales, dy_perm,
+                                   dout, dx_perm, dx_shared, ws, stream=None):
+    """Dgrad of every expert FFN in FP8 (gradients in 1 x 128 tiles along
+    their GEMM's contraction, weights in their forward blocks)."""
+    opt = dict(allow_none=True)
+    _check("moe_experts_backward_input_fp8", _lib.moe_experts_backward_input_fp8(
+        _cfg(cfg), _ptr(x_perm, "x_perm", _F8), _ptr(x_perm_scales, "x_perm_scales", torch.float32),
+        _ptr(x_q, "x_q", _F8, **opt), _ptr(x_q_scales, "x_q_scales", torch.float32, **opt),
+        _ptr(offsets, "offsets", torch.int32),
+        _ptr(w13, "w13", _F8), _ptr(w13_scales, "w13_scales", torch.float32),
+        _ptr(w13t, "w13t", _F8), _ptr(w13t_scales, "w13t_scales", torch.float32),
+        _ptr(w2t, "w2t", _F8), _ptr(w2t_scales, "w2t_scales", torch.float32),
+        _ptr(ws13, "ws13", _F8, **opt), _ptr(ws13_scales, "ws13_scales", torch.float32, **opt),
+        _ptr(ws13t, "ws13t", _F8, **opt), _ptr(ws13t_scales, "ws13t_scales", torch.float32, **opt),
+        _ptr(ws2t, "ws2t", _F8, **opt), _ptr(ws2t_scales, "ws2t_scales", torch.float32, **opt),
+        _ptr(dy_perm, "dy_perm", _BF), _ptr(dout, "dout", _BF, **opt),
+        _ptr(dx_perm, "dx_perm", _BF), _ptr(dx_shared, "dx_shared", _BF, **opt),
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
 

@@ -127,6 +127,38 @@ struct ExpertsBwdArgs {
   ExpertsBwdScratch scratch;
 };
 
+// Backward for input of the FP8 expert FFNs (backward_fp8.cu).
+struct ExpertsBwdFp8Args {
+  const moe_cfg_t* cfg;
+  const void* x_perm;          // forward's E4M3 rows [T*K, d] and 1 x 128 scales
+  const float* x_perm_scales;
+  const void* x_q;             // forward's E4M3 token rows [T, d] (shared expert)
+  const float* x_q_scales;
+  const int32_t* offsets;
+  const void* w13;             // [E, 2I, d] codes, [E, 2I/128, d/128] scales
+  const float* w13_scales;
+  const void* w13t;            // [E, d, 2I] transposed codes and block scales
+  const float* w13t_scales;
+  const void* w2t;             // [E, I, d] transposed W2 codes and block scales
+  const float* w2t_scales;
+  const void* ws13;            // the shared expert's: [1, 2I, d], [1, d, 2I], [1, I, d]
+  const float* ws13_scales;
+  const void* ws13t;
+  const float* ws13t_scales;
+  const void* ws2t;
+  const float* ws2t_scales;
+  const void* dy_perm;         // [T*K, d] bf16
+  const void* dout;            // [T, d] bf16
+  void* dx_perm;               // [T*K, d] bf16 out
+  void* dx_shared;             // [T, d] bf16 out
+  void* ws;                    // experts_bwd_fp8_scratch_bytes
+};
+size_t experts_bwd_fp8_scratch_bytes(const moe_cfg_t& c);
+cudaError_t launch_experts_bwd_input_fp8(const ExpertsBwdFp8Args& a, cudaStream_t s);
+cudaError_t launch_transpose_weights_fp8(const void* w_q, const float* w_scales, int n_mats,
+                                         int rows, int cols, void* wt_q, float* wt_scales,
+                                         cudaStream_t s);
+
 struct RouteBwdArgs {
   const void* x;
   const float* router_w;

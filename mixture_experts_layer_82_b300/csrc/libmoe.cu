@@ -9,5 +9,6 @@
 #include "experts_fp8.cu"
 #include "backward_sm100.cu"
 #include "backward.cu"
+#include "backward_fp8.cu"
 #include "tma.cu"
 #include "route_static.cu"

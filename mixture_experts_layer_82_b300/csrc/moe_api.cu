@@ -316,11 +316,20 @@ moe_status_t moe_balance_stat(const moe_cfg_t* cfg, const float* affinity,
 // ------------------------------------------------------------ backward pass
 namespace {
 
+// The backward calls: the bf16 kind (up to 64 shared experts) and, for the
+// calls that handle it, the FP8 kind (at most one shared expert).
 moe_status_t check_backward_cfg(const moe_cfg_t* cfg) {
   moe_status_t st = moe_check_cfg(cfg);
   if (st != MOE_OK) return st;
-  if (cfg->dtype != MOE_DTYPE_BF16 || cfg->n_shared > 64) return MOE_ERR_SHAPE;
-  return MOE_OK;
+  if (cfg->dtype == MOE_DTYPE_BF16) return cfg->n_shared > 64 ? MOE_ERR_SHAPE : MOE_OK;
+  if (cfg->dtype == MOE_DTYPE_FP8_E4M3) return cfg->n_shared > 1 ? MOE_ERR_SHAPE : MOE_OK;
+  return MOE_ERR_SHAPE;
+}
+
+// Bytes of the expert part of the backward workspace (the routing part follows).
+size_t backward_experts_bytes(const moe_cfg_t& c) {
+  return c.dtype == MOE_DTYPE_FP8_E4M3 ? experts_bwd_fp8_scratch_bytes(c)
+                                       : experts_bwd_scratch_bytes(c);
 }
 
 size_t backward_route_bytes(const moe_cfg_t& c) {
@@ -331,7 +340,7 @@ size_t backward_route_bytes(const moe_cfg_t& c) {
 
 size_t moe_backward_workspace_bytes(const moe_cfg_t* c) {
   if (check_backward_cfg(c) != MOE_OK) return 0;
-  return experts_bwd_scratch_bytes(*c) + backward_route_bytes(*c);
+  return backward_experts_bytes(*c) + backward_route_bytes(*c);
 }
 
 moe_status_t moe_combine_backward(const moe_cfg_t* cfg, const void* dout, const void* y_perm,
@@ -355,6 +364,7 @@ moe_status_t moe_experts_grouped_train(const moe_cfg_t* cfg, const void* x_perm,
                                        void* y_shared, void* ws, size_t ws_bytes, void* bws,
                                        size_t bws_bytes, void* stream) {
   moe_status_t st = check_backward_cfg(cfg);
+  if (st == MOE_OK && cfg->dtype != MOE_DTYPE_BF16) st = MOE_ERR_SHAPE;  // bf16 kind only
   if (st != MOE_OK) return st;
   const moe_cfg_t& c = *cfg;
   if (x_perm == nullptr || offsets == nullptr || w13 == nullptr || w2 == nullptr ||
@@ -386,6 +396,7 @@ moe_status_t moe_experts_backward_input(const moe_cfg_t* cfg, const void* x_perm
                                         void* dx_shared, int32_t ab_kept, void* ws,
                                         size_t ws_bytes, void* stream) {
   moe_status_t st = check_backward_cfg(cfg);
+  if (st == MOE_OK && cfg->dtype != MOE_DTYPE_BF16) st = MOE_ERR_SHAPE;  // bf16 kind only
   if (st != MOE_OK) return st;
   const moe_cfg_t& c = *cfg;
   if (x_perm == nullptr || offsets == nullptr || w13 == nullptr || w2 == nullptr ||
@@ -416,6 +427,7 @@ moe_status_t moe_experts_backward_weights(const moe_cfg_t* cfg, const void* x_pe
                                           void* dw2, void* dws13, void* dws2, void* ws,
                                           size_t ws_bytes, void* stream) {
   moe_status_t st = check_backward_cfg(cfg);
+  if (st == MOE_OK && cfg->dtype != MOE_DTYPE_BF16) st = MOE_ERR_SHAPE;  // bf16 kind only
   if (st != MOE_OK) return st;
   const moe_cfg_t& c = *cfg;
   if (x_perm == nullptr || offsets == nullptr || dy_perm == nullptr || dw13 == nullptr ||
@@ -465,9 +477,65 @@ moe_status_t moe_route_backward(const moe_cfg_t* cfg, const void* x, const float
   a.offsets = offsets; a.dx_perm = dx_perm;
   a.dx_shared = c.n_shared > 0 ? dx_shared : nullptr;
   a.dlogit = dlogit;
-  a.dlogit_row = reinterpret_cast<float*>(static_cast<char*>(ws) + experts_bwd_scratch_bytes(c));
+  a.dlogit_row = reinterpret_cast<float*>(static_cast<char*>(ws) + backward_experts_bytes(c));
   a.dx = dx; a.drouter_w = drouter_w;
   return from_cuda(launch_route_backward(c, a, as_stream(stream)));
+}
+
+moe_status_t moe_transpose_weights_fp8(const void* w_q, const float* w_scales, int32_t n_mats,
+                                       int32_t rows, int32_t cols, void* wt_q, float* wt_scales,
+                                       void* stream) {
+  if (w_q == nullptr || w_scales == nullptr || wt_q == nullptr || wt_scales == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (n_mats < 1 || rows < 1 || cols < 1) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 != 0 || cols % 128 != 0) return MOE_ERR_SHAPE;
+  const void* ptrs[] = {w_q, w_scales, wt_q, wt_scales};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  return from_cuda(launch_transpose_weights_fp8(w_q, w_scales, n_mats, rows, cols, wt_q, wt_scales,
+                                                as_stream(stream)));
+}
+
+moe_status_t moe_experts_backward_input_fp8(
+    const moe_cfg_t* cfg, const void* x_perm, const float* x_perm_scales, const void* x_q,
+    const float* x_q_scales, const int32_t* offsets, const void* w13, const float* w13_scales,
+    const void* w13t, const float* w13t_scales, const void* w2t, const float* w2t_scales,
+    const void* ws13, const float* ws13_scales, const void* ws13t, const float* ws13t_scales,
+    const void* ws2t, const float* ws2t_scales, const void* dy_perm, const void* dout,
+    void* dx_perm, void* dx_shared, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (c.dtype != MOE_DTYPE_FP8_E4M3 || c.n_shared > 1) return MOE_ERR_SHAPE;
+  // (its scratch is the expert part of the backward workspace)
+  const void* need[] = {x_perm, x_perm_scales, offsets, w13, w13_scales, w13t, w13t_scales,
+                        w2t, w2t_scales, dy_perm, dx_perm, ws};
+  for (const void* p : need)
+    if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0) {
+    const void* need_sh[] = {x_q, x_q_scales, ws13, ws13_scales, ws13t, ws13t_scales, ws2t,
+                             ws2t_scales, dout, dx_shared};
+    for (const void* p : need_sh)
+      if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  }
+  const void* ptrs[] = {x_perm, x_perm_scales, x_q, x_q_scales, offsets, w13, w13_scales,
+                        w13t, w13t_scales, w2t, w2t_scales, ws13, ws13_scales, ws13t,
+                        ws13t_scales, ws2t, ws2t_scales, dy_perm, dout, dx_perm, dx_shared, ws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  if (ws_bytes < experts_bwd_fp8_scratch_bytes(c)) return MOE_ERR_WORKSPACE;
+  ExpertsBwdFp8Args a{};
+  a.cfg = &c;
+  a.x_perm = x_perm; a.x_perm_scales = x_perm_scales; a.x_q = x_q; a.x_q_scales = x_q_scales;
+  a.offsets = offsets;
+  a.w13 = w13; a.w13_scales = w13_scales; a.w13t = w13t; a.w13t_scales = w13t_scales;
+  a.w2t = w2t; a.w2t_scales = w2t_scales;
+  a.ws13 = ws13; a.ws13_scales = ws13_scales; a.ws13t = ws13t; a.ws13t_scales = ws13t_scales;
+  a.ws2t = ws2t; a.ws2t_scales = ws2t_scales;
+  a.dy_perm = dy_perm; a.dout = dout; a.dx_perm = dx_perm;
+  a.dx_shared = c.n_shared > 0 ? dx_shared : nullptr;
+  a.ws = ws;
+  return from_cuda(launch_experts_bwd_input_fp8(a, as_stream(stream)));
 }
 
 moe_status_t moe_quantize_weights_fp8(const void* w_bf16, int32_t n_mats, int32_t rows,

@@ -12,7 +12,16 @@ from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_expert
                moe_experts_grouped_gated,
                moe_combine, moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes,
                moe_backward_workspace_bytes, moe_combine_backward, moe_experts_backward_input,
-               moe_experts_backward_weights, moe_route_backward, moe_experts_grouped_train)
+               moe_experts_backward_weights, moe_route_backward, moe_experts_grouped_train,
+               moe_transpose_weights_fp8, moe_experts_backward_input_fp8)
+
+
+def _transpose_fp8(q, s, stream=None):
+    n, rows, cols = q.shape
+    qt = torch.empty(n, cols, rows, dtype=q.dtype, device=q.device)
+    st = torch.empty(n, cols // 128, rows // 128, dtype=torch.float32, device=q.device)
+    moe_transpose_weights_fp8(q, s, qt, st, stream=stream)
+    return qt, st
 
 
 def _quantize(w, stream=None):
@@ -150,6 +159,16 @@ class MoELayer:
         T, d, E, K, I, ns = c.T, c.d, c.E, c.k, c.inter, c.n_shared
         bf = dict(dtype=torch.bfloat16, device=dev)
         f32 = dict(dtype=torch.float32, device=dev)
+        if c.dtype == "fp8":
+            # Dgrad reads the weights contracted over their other dimension:
+            # transposed copies of the forward's codes and blocks
+            self.w13t, self.w13t_s = _transpose_fp8(self.w13, self.w13_s)
+            self.w2t, self.w2t_s = _transpose_fp8(self.w2, self.w2_s)
+            if ns:
+                self.ws13t, self.ws13t_s = _transpose_fp8(self.ws13, self.ws13_s)
+                self.ws2t, self.ws2t_s = _transpose_fp8(self.ws2, self.ws2_s)
+            else:
+                self.ws13t = self.ws13t_s = self.ws2t = self.ws2t_s = None
         self.dy_perm = torch.empty(T * K, d, **bf)
         self.dgate = torch.empty(T, K, **f32)
         self.dx_perm = torch.empty(T * K, d, **bf)
@@ -157,13 +176,16 @@ class MoELayer:
         self.dlogit = torch.empty(T, K, **f32)
         self.dx = torch.empty(T, d, **bf)
         self.drouter_w = torch.empty(E, d, **f32)
-        self.dw13 = torch.empty(E, 2 * I, d, **bf)
-        self.dw2 = torch.empty(E, d, I, **bf)
-        self.dws13 = torch.empty(ns, 2 * I, d, **bf) if ns else None
-        self.dws2 = torch.empty(ns, d, I, **bf) if ns else None
+        if c.dtype == "bf16":
+            self.dw13 = torch.empty(E, 2 * I, d, **bf)
+            self.dw2 = torch.empty(E, d, I, **bf)
+            self.dws13 = torch.empty(ns, 2 * I, d, **bf) if ns else None
+            self.dws2 = torch.empty(ns, d, I, **bf) if ns else None
+        else:
+            self.dw13 = self.dw2 = self.dws13 = self.dws2 = None
         self.bws = torch.empty(moe_backward_workspace_bytes(c), dtype=torch.uint8, device=dev)
 
-    def backward(self, x, dout, affinity, stream=None, weights=True, events=None):
+    def backward(self, x, dout, affinity, stream=None, weights=None, events=None):
         """Backward of the last ``forward(x, affinity_out=affinity)`` (bf16
         kind; with ``keep=True`` there, the gate/up products are not
         recomputed), given ``dout`` = dL/dy [T, d] bf16.  Fills ``dx``,
@@ -172,12 +194,37 @@ class MoELayer:
         ``dx_perm``, ``dx_shared``); returns ``dx``.  The selection and the
         bias are those of the forward; the bias gets no gradient.
         ``events`` (four torch.cuda.Event) are recorded on ``stream`` around
-        the expert Dgrad call and around the expert Wgrad call."""
+        the expert Dgrad call and around the expert Wgrad call.
+
+        FP8 kind: the input side only (``weights`` must stay False): the
+        expert Dgrad GEMMs run in FP8 on the forward's codes
+        (moe_experts_backward_input_fp8) and give ``dx``, ``drouter_w``."""
         c = self.cfg
-        if c.dtype != "bf16":
-            raise ValueError("the backward pass is implemented for the bf16 kind")
+        if c.dtype not in ("bf16", "fp8"):
+            raise ValueError("the backward pass is implemented for the bf16 and fp8 kinds")
+        if weights is None:
+            weights = c.dtype == "bf16"
+        if weights and c.dtype != "bf16":
+            raise ValueError("the weight gradients are implemented for the bf16 kind")
         if not hasattr(self, "bws"):
             self._grad_buffers()
+        if c.dtype == "fp8":
+            moe_combine_backward(c, dout, self.y_perm, self.row_of_slot, self.topk_w,
+                                 self.dy_perm, self.dgate, stream=stream)
+            if events is not None:
+                events[0].record(stream)
+            moe_experts_backward_input_fp8(
+                c, self.x_perm, self.x_perm_s, self.x_q, self.x_q_s, self.offsets, self.w13,
+                self.w13_s, self.w13t, self.w13t_s, self.w2t, self.w2t_s, self.ws13, self.ws13_s,
+                self.ws13t, self.ws13t_s, self.ws2t, self.ws2t_s, self.dy_perm, dout,
+                self.dx_perm, self.dx_shared, self.bws, stream=stream)
+            if events is not None:
+                events[1].record(stream)
+            moe_route_backward(c, x, self.router_w, affinity, self.topk_idx, self.dgate,
+                               self.row_of_slot, self.token_of_row, self.offsets, self.dx_perm,
+                               self.dx_shared, self.dlogit, self.dx, self.drouter_w, self.bws,
+                               stream=stream)
+            return self.dx
         if self.gather:
             # the gathering forward never wrote the permuted rows
             moe_permute(c, x, self.token_of_row, self.x_perm, stream=stream)

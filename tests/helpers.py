@@ -23,18 +23,20 @@ def row_errors(a, b):
     return np.linalg.norm(a - b, axis=1) / np.maximum(nb, floor)
 
 
-def assert_close(a, b, tol, what=None):
-    """Both the whole tensor (relative Frobenius error) and each row on its
-    own (see row_errors) within `tol`: a single bad row of a large tensor
-    hardly moves the Frobenius norm, so every row is bounded too."""
+def assert_close(a, b, tol, what=None, row_tol=None):
+    """Both the whole tensor (relative Frobenius error) within `tol` and each
+    row on its own (see row_errors) within `row_tol` (default `tol`): a
+    single bad row of a large tensor hardly moves the Frobenius norm, so
+    every row is bounded too."""
+    row_tol = tol if row_tol is None else row_tol
     fro = rel_frobenius(a, b)
     if len(np.shape(b)) == 0 or np.size(b) == 0:
         assert fro < tol, (what, fro)
         return
     r = row_errors(a, b)
     worst = int(np.argmax(r))
-    assert fro < tol and r[worst] < tol, (what, f"frobenius {fro:.3e}",
-                                          f"worst row {worst}: {r[worst]:.3e}")
+    assert fro < tol and r[worst] < row_tol, (what, f"frobenius {fro:.3e}",
+                                              f"worst row {worst}: {r[worst]:.3e}")
 
 
 def host(t):

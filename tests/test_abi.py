@@ -151,9 +151,17 @@ def test_backward_workspace_formula_and_kinds():
     tk, T, I, ns = c.T * c.k, c.T, c.inter, c.n_shared
     assert moe.moe_backward_workspace_bytes(c) == (_align256((tk + T * ns) * 3 * I * 2)
                                                    + _align256(tk * 4))
-    # the backward exists for the bf16 kind only, and for at most 64 shared experts
+    # the backward exists for the bf16 kind (at most 64 shared experts) and,
+    # on the input side, the FP8 kind with at most one shared expert: its
+    # expert part holds q(dy), [a | b], dh and q([da | db]) for T*K + T rows
     assert moe.moe_backward_workspace_bytes(_base(dtype="fp32")) == 0
-    assert moe.moe_backward_workspace_bytes(_base(dtype="fp8")) == 0
+    assert moe.moe_backward_workspace_bytes(_base(dtype="fp8")) == 0   # two shared experts
+    f = _base(dtype="fp8", n_shared=1)
+    rows, d = tk + T, f.d
+    assert moe.moe_backward_workspace_bytes(f) == (
+        _align256(rows * d) + _align256(rows * (d // 128) * 4) + _align256(rows * 2 * I * 2)
+        + _align256(rows * I * 2) + _align256(rows * 2 * I) + _align256(rows * (2 * I // 128) * 4)
+        + _align256(tk * 4))
     assert moe.moe_backward_workspace_bytes(_base(n_shared=65)) == 0
     assert moe.moe_backward_workspace_bytes(_base(d=2000)) == 0
 
