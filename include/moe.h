@@ -341,7 +341,8 @@ moe_status_t moe_balance_stat(const moe_cfg_t* cfg, const float* affinity,
  * survive from moe_experts_backward_input to moe_experts_backward_weights).
  * FP8 kind (N_s <= 1): the buffers of moe_experts_backward_input_fp8 for
  * T*K + T rows (q(dy) codes and scales, [a | b] and dh in bf16, q([da | db])
- * codes and scales).  0 for a configuration the backward does not support.
+ * codes and scales), then those of moe_experts_backward_weights_fp8 (the
+ * segments' padded starts and the four transposed 128 x 1-tile operands).  0 for a configuration the backward does not support.
  * moe_combine_backward and moe_route_backward take both kinds (their data
  * are bf16 in both); the other backward calls name their kind. */
 size_t moe_backward_workspace_bytes(const moe_cfg_t* cfg);
@@ -473,8 +474,8 @@ moe_status_t moe_transpose_weights_fp8(const void* w_q, const float* w_scales,
  *   dout    [T, d] bf16      dL/dy of the layer (the shared expert's dy)
  *   dx_perm [T*K, d] bf16 out, dx_shared [T, d] bf16 out (NULL if N_s = 0)
  *   ws, ws_bytes             at least moe_backward_workspace_bytes(cfg)
- * FP8 kind with at most one shared expert (MOE_ERR_SHAPE otherwise).  The
- * weight gradients of the FP8 kind are not computed by this library.
+ * FP8 kind with at most one shared expert (MOE_ERR_SHAPE otherwise).  It
+ * leaves [a | b] and dh in `ws` for moe_experts_backward_weights_fp8.
  */
 moe_status_t moe_experts_backward_input_fp8(
     const moe_cfg_t* cfg, const void* x_perm, const float* x_perm_scales, const void* x_q,
@@ -483,6 +484,32 @@ moe_status_t moe_experts_backward_input_fp8(
     const void* ws13, const float* ws13_scales, const void* ws13t, const float* ws13t_scales,
     const void* ws2t, const float* ws2t_scales, const void* dy_perm, const void* dout,
     void* dx_perm, void* dx_shared, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_experts_backward_weights_fp8 - Wgrad of every expert FFN in FP8 E4M3
+ * (mixed precision framework paragraph: Wgrad in FP8 with fp32
+ * accumulation).  The contraction runs over the token rows of each segment,
+ * so both operands are quantised in 128 x 1 tiles (128 consecutive rows of
+ * one column, scale fl32(amax / 448); a segment's last tile holds the rows
+ * it has):
+ *   dW2 = q(dy)^T q(h),   dW13 = q([da | db])^T q(u)
+ * with u the dequantised forward codes and h, [da | db] formed (fp32) from
+ * the [a | b] and dh that moe_experts_backward_input_fp8 left in `ws`; every
+ * 128-row partial is promoted to fp32 with both tiles' scales.
+ *   x_perm, x_perm_scales, x_q, x_q_scales, offsets  as for the input call
+ *   dy_perm [T*K, d], dout [T, d]  bf16, as for the input call
+ *   dw13 [E, 2I, d], dw2 [E, d, I]  bf16 out (zeros for an expert with no rows)
+ *   dws13 [1, 2I, d], dws2 [1, d, I] bf16 out (NULL if N_s = 0)
+ *   ws, ws_bytes  the workspace of this step's input call (untouched in
+ *                 between except by moe_route_backward)
+ * Each operand is first written transposed, every segment padded to whole
+ * 128-row tiles, so that each K block of the GEMM starts on an aligned
+ * boundary; moe_backward_workspace_bytes covers those copies.
+ */
+moe_status_t moe_experts_backward_weights_fp8(
+    const moe_cfg_t* cfg, const void* x_perm, const float* x_perm_scales, const void* x_q,
+    const float* x_q_scales, const int32_t* offsets, const void* dy_perm, const void* dout,
+    void* dw13, void* dw2, void* dws13, void* dws2, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * moe_quantize_weights_fp8 - offline utility: quantise `n_mats` bf16

@@ -43,7 +43,7 @@ EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_byt
             "moe_selftest_wait", "moe_backward_workspace_bytes", "moe_combine_backward",
             "moe_experts_backward_input", "moe_experts_backward_weights", "moe_route_backward",
             "moe_experts_grouped_train", "moe_experts_grouped_gated", "moe_transpose_weights_fp8",
-            "moe_experts_backward_input_fp8")
+            "moe_experts_backward_input_fp8", "moe_experts_backward_weights_fp8")
 
 
 class MoeCfg(ctypes.Structure):
@@ -114,6 +114,8 @@ _lib.moe_transpose_weights_fp8.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int3
                                            _P, _P, _P]
 _lib.moe_experts_backward_input_fp8.restype = ctypes.c_int
 _lib.moe_experts_backward_input_fp8.argtypes = [_CFG] + [_P] * 21 + [_P, ctypes.c_size_t, _P]
+_lib.moe_experts_backward_weights_fp8.restype = ctypes.c_int
+_lib.moe_experts_backward_weights_fp8.argtypes = [_CFG] + [_P] * 11 + [_P, ctypes.c_size_t, _P]
 
 
 def library():
@@ -424,6 +426,20 @@ def moe_experts_backward_input_fp8(cfg, x_perm, x_perm_scales, x_q, x_q_scales, 
         _ptr(ws2t, "ws2t", _F8, **opt), _ptr(ws2t_scales, "ws2t_scales", torch.float32, **opt),
         _ptr(dy_perm, "dy_perm", _BF), _ptr(dout, "dout", _BF, **opt),
         _ptr(dx_perm, "dx_perm", _BF), _ptr(dx_shared, "dx_shared", _BF, **opt),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_experts_backward_weights_fp8(cfg, x_perm, x_perm_scales, x_q, x_q_scales, offsets,
+                                     dy_perm, dout, dw13, dw2, dws13, dws2, ws, stream=None):
+    """Wgrad of every expert FFN in FP8 (both operands in 128 x 1 tiles along
+    the segment's rows), after moe_experts_backward_input_fp8 on ``ws``."""
+    opt = dict(allow_none=True)
+    _check("moe_experts_backward_weights_fp8", _lib.moe_experts_backward_weights_fp8(
+        _cfg(cfg), _ptr(x_perm, "x_perm", _F8), _ptr(x_perm_scales, "x_perm_scales", torch.float32),
+        _ptr(x_q, "x_q", _F8, **opt), _ptr(x_q_scales, "x_q_scales", torch.float32, **opt),
+        _ptr(offsets, "offsets", torch.int32), _ptr(dy_perm, "dy_perm", _BF),
+        _ptr(dout, "dout", _BF, **opt), _ptr(dw13, "dw13", _BF), _ptr(dw2, "dw2", _BF),
+        _ptr(dws13, "dws13", _BF, **opt), _ptr(dws2, "dws2", _BF, **opt),
         _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
 

@@ -230,6 +230,13 @@ cudaError_t run_fp8_gemm(const moe_cfg_t& c, const int32_t* offsets, const Fp8Ge
 
 }  // namespace bwdfp8
 
+void experts_bwd_fp8_ab_dh(const moe_cfg_t& c, void* ws, const __nv_bfloat16** ab,
+                           const __nv_bfloat16** dh) {
+  const bwdfp8::Fp8BwdScratch s = bwdfp8::carve_fp8_bwd(c, ws);
+  *ab = s.ab;
+  *dh = s.dh;
+}
+
 cudaError_t launch_experts_bwd_input_fp8(const ExpertsBwdFp8Args& a, cudaStream_t st) {
   using namespace bwdfp8;
   const moe_cfg_t& c = *a.cfg;

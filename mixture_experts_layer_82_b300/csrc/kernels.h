@@ -154,6 +154,33 @@ struct ExpertsBwdFp8Args {
   void* ws;                    // experts_bwd_fp8_scratch_bytes
 };
 size_t experts_bwd_fp8_scratch_bytes(const moe_cfg_t& c);
+
+// Backward for weights of the FP8 expert FFNs (backward_fp8_wgrad.cu): from
+// the forward's codes, the caller's dy and the [a | b] and dh the input
+// side left in its scratch.
+struct ExpertsBwdWeightsFp8Args {
+  const moe_cfg_t* cfg;
+  const void* x_perm;
+  const float* x_perm_scales;
+  const void* x_q;
+  const float* x_q_scales;
+  const int32_t* offsets;
+  const void* dy_perm;
+  const void* dout;
+  const __nv_bfloat16* ab;  // [T*K + T, 2I]
+  const __nv_bfloat16* dh;  // [T*K + T, I]
+  void* dw13;               // [E, 2I, d] bf16 out
+  void* dw2;                // [E, d, I] bf16 out
+  void* dws13;              // [1, 2I, d], [1, d, I] (N_s = 1)
+  void* dws2;
+  void* wg_ws;              // experts_wgrad_fp8_scratch_bytes
+};
+size_t experts_wgrad_fp8_scratch_bytes(const moe_cfg_t& c);
+cudaError_t launch_experts_bwd_weights_fp8(const ExpertsBwdWeightsFp8Args& a, cudaStream_t s);
+// [a | b] and dh of the routed rows in the FP8 input side's scratch (the
+// shared expert's rows follow them).
+void experts_bwd_fp8_ab_dh(const moe_cfg_t& c, void* ws, const __nv_bfloat16** ab,
+                           const __nv_bfloat16** dh);
 cudaError_t launch_experts_bwd_input_fp8(const ExpertsBwdFp8Args& a, cudaStream_t s);
 cudaError_t launch_transpose_weights_fp8(const void* w_q, const float* w_scales, int n_mats,
                                          int rows, int cols, void* wt_q, float* wt_scales,

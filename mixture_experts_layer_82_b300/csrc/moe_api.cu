@@ -328,8 +328,9 @@ moe_status_t check_backward_cfg(const moe_cfg_t* cfg) {
 
 // Bytes of the expert part of the backward workspace (the routing part follows).
 size_t backward_experts_bytes(const moe_cfg_t& c) {
-  return c.dtype == MOE_DTYPE_FP8_E4M3 ? experts_bwd_fp8_scratch_bytes(c)
-                                       : experts_bwd_scratch_bytes(c);
+  return c.dtype == MOE_DTYPE_FP8_E4M3
+             ? experts_bwd_fp8_scratch_bytes(c) + experts_wgrad_fp8_scratch_bytes(c)
+             : experts_bwd_scratch_bytes(c);
 }
 
 size_t backward_route_bytes(const moe_cfg_t& c) {
@@ -536,6 +537,39 @@ moe_status_t moe_experts_backward_input_fp8(
   a.dx_shared = c.n_shared > 0 ? dx_shared : nullptr;
   a.ws = ws;
   return from_cuda(launch_experts_bwd_input_fp8(a, as_stream(stream)));
+}
+
+moe_status_t moe_experts_backward_weights_fp8(
+    const moe_cfg_t* cfg, const void* x_perm, const float* x_perm_scales, const void* x_q,
+    const float* x_q_scales, const int32_t* offsets, const void* dy_perm, const void* dout,
+    void* dw13, void* dw2, void* dws13, void* dws2, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (c.dtype != MOE_DTYPE_FP8_E4M3 || c.n_shared > 1) return MOE_ERR_SHAPE;
+  const void* need[] = {x_perm, x_perm_scales, offsets, dy_perm, dw13, dw2, ws};
+  for (const void* p : need)
+    if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0) {
+    const void* need_sh[] = {x_q, x_q_scales, dout, dws13, dws2};
+    for (const void* p : need_sh)
+      if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  }
+  const void* ptrs[] = {x_perm, x_perm_scales, x_q, x_q_scales, offsets, dy_perm, dout,
+                        dw13, dw2, dws13, dws2, ws};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_ALIGN;
+  if (ws_bytes < moe_backward_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  ExpertsBwdWeightsFp8Args a{};
+  a.cfg = &c;
+  a.x_perm = x_perm; a.x_perm_scales = x_perm_scales; a.x_q = x_q; a.x_q_scales = x_q_scales;
+  a.offsets = offsets; a.dy_perm = dy_perm; a.dout = dout;
+  experts_bwd_fp8_ab_dh(c, ws, &a.ab, &a.dh);
+  a.dw13 = dw13; a.dw2 = dw2;
+  a.dws13 = c.n_shared > 0 ? dws13 : nullptr;
+  a.dws2 = c.n_shared > 0 ? dws2 : nullptr;
+  a.wg_ws = static_cast<char*>(ws) + experts_bwd_fp8_scratch_bytes(c);
+  return from_cuda(launch_experts_bwd_weights_fp8(a, as_stream(stream)));
 }
 
 moe_status_t moe_quantize_weights_fp8(const void* w_bf16, int32_t n_mats, int32_t rows,

@@ -13,7 +13,8 @@ from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_expert
                moe_combine, moe_bias_update, moe_quantize_weights_fp8, moe_workspace_bytes,
                moe_backward_workspace_bytes, moe_combine_backward, moe_experts_backward_input,
                moe_experts_backward_weights, moe_route_backward, moe_experts_grouped_train,
-               moe_transpose_weights_fp8, moe_experts_backward_input_fp8)
+               moe_transpose_weights_fp8, moe_experts_backward_input_fp8,
+               moe_experts_backward_weights_fp8)
 
 
 def _transpose_fp8(q, s, stream=None):
@@ -176,16 +177,13 @@ class MoELayer:
         self.dlogit = torch.empty(T, K, **f32)
         self.dx = torch.empty(T, d, **bf)
         self.drouter_w = torch.empty(E, d, **f32)
-        if c.dtype == "bf16":
-            self.dw13 = torch.empty(E, 2 * I, d, **bf)
-            self.dw2 = torch.empty(E, d, I, **bf)
-            self.dws13 = torch.empty(ns, 2 * I, d, **bf) if ns else None
-            self.dws2 = torch.empty(ns, d, I, **bf) if ns else None
-        else:
-            self.dw13 = self.dw2 = self.dws13 = self.dws2 = None
+        self.dw13 = torch.empty(E, 2 * I, d, **bf)
+        self.dw2 = torch.empty(E, d, I, **bf)
+        self.dws13 = torch.empty(ns, 2 * I, d, **bf) if ns else None
+        self.dws2 = torch.empty(ns, d, I, **bf) if ns else None
         self.bws = torch.empty(moe_backward_workspace_bytes(c), dtype=torch.uint8, device=dev)
 
-    def backward(self, x, dout, affinity, stream=None, weights=None, events=None):
+    def backward(self, x, dout, affinity, stream=None, weights=True, events=None):
         """Backward of the last ``forward(x, affinity_out=affinity)`` (bf16
         kind; with ``keep=True`` there, the gate/up products are not
         recomputed), given ``dout`` = dL/dy [T, d] bf16.  Fills ``dx``,
@@ -196,16 +194,12 @@ class MoELayer:
         ``events`` (four torch.cuda.Event) are recorded on ``stream`` around
         the expert Dgrad call and around the expert Wgrad call.
 
-        FP8 kind: the input side only (``weights`` must stay False): the
-        expert Dgrad GEMMs run in FP8 on the forward's codes
-        (moe_experts_backward_input_fp8) and give ``dx``, ``drouter_w``."""
+        FP8 kind: the expert Dgrad and Wgrad GEMMs run in FP8 on the
+        forward's codes (moe_experts_backward_input_fp8,
+        moe_experts_backward_weights_fp8); at most one shared expert."""
         c = self.cfg
         if c.dtype not in ("bf16", "fp8"):
             raise ValueError("the backward pass is implemented for the bf16 and fp8 kinds")
-        if weights is None:
-            weights = c.dtype == "bf16"
-        if weights and c.dtype != "bf16":
-            raise ValueError("the weight gradients are implemented for the bf16 kind")
         if not hasattr(self, "bws"):
             self._grad_buffers()
         if c.dtype == "fp8":
@@ -224,6 +218,15 @@ class MoELayer:
                                self.row_of_slot, self.token_of_row, self.offsets, self.dx_perm,
                                self.dx_shared, self.dlogit, self.dx, self.drouter_w, self.bws,
                                stream=stream)
+            if weights:
+                if events is not None:
+                    events[2].record(stream)
+                moe_experts_backward_weights_fp8(
+                    c, self.x_perm, self.x_perm_s, self.x_q, self.x_q_s, self.offsets,
+                    self.dy_perm, dout, self.dw13, self.dw2, self.dws13, self.dws2, self.bws,
+                    stream=stream)
+                if events is not None:
+                    events[3].record(stream)
             return self.dx
         if self.gather:
             # the gathering forward never wrote the permuted rows

@@ -157,11 +157,18 @@ def test_backward_workspace_formula_and_kinds():
     assert moe.moe_backward_workspace_bytes(_base(dtype="fp32")) == 0
     assert moe.moe_backward_workspace_bytes(_base(dtype="fp8")) == 0   # two shared experts
     f = _base(dtype="fp8", n_shared=1)
-    rows, d = tk + T, f.d
-    assert moe.moe_backward_workspace_bytes(f) == (
-        _align256(rows * d) + _align256(rows * (d // 128) * 4) + _align256(rows * 2 * I * 2)
-        + _align256(rows * I * 2) + _align256(rows * 2 * I) + _align256(rows * (2 * I // 128) * 4)
-        + _align256(tk * 4))
+    rows, d, E = tk + T, f.d, f.E
+    dgrad = (_align256(rows * d) + _align256(rows * (d // 128) * 4) + _align256(rows * 2 * I * 2)
+             + _align256(rows * I * 2) + _align256(rows * 2 * I)
+             + _align256(rows * (2 * I // 128) * 4))
+    # Wgrad: padded segment starts, then dy, u, h, [da | db] transposed with
+    # every segment padded to 128 rows (routed) and the shared expert's T rows
+    P = (tk + 127 * E + 127) // 128 * 128
+    Ps = (T + 127) // 128 * 128
+    wgrad = _align256((E + 1) * 4) + sum(
+        _align256(C * P) + _align256(P // 128 * C * 4) + _align256(C * Ps)
+        + _align256(Ps // 128 * C * 4) for C in (d, d, I, 2 * I))
+    assert moe.moe_backward_workspace_bytes(f) == dgrad + wgrad + _align256(tk * 4)
     assert moe.moe_backward_workspace_bytes(_base(n_shared=65)) == 0
     assert moe.moe_backward_workspace_bytes(_base(d=2000)) == 0
 
