@@ -17,9 +17,11 @@ sum their per-expert loads with one all-reduce of counts[E] per step so that
 the bias update sees the whole batch); the time is the maximum over ranks.
 Rank 0 prints one JSON line.
 
-``--train`` (bf16 kind) makes a step one training pass instead: the forward
-above, then its backward (combine backward, expert Dgrad with the gate/up
-products recomputed, router backward, expert Wgrad), given a fixed dL/dy.
+``--train`` (bf16 and fp8 kinds) makes a step one training pass instead: the
+forward above, then its backward (combine backward, expert Dgrad, router
+backward, expert Wgrad), given a fixed dL/dy.  The bf16 forward keeps the
+gate/up products for the backward; the FP8 backward recomputes them from the
+forward's codes.
 
 ``--impl reference`` times the CPU oracle (fp64 NumPy) on the host cores on a
 bounded sample of the same workload; that is the only other place, besides
@@ -98,7 +100,14 @@ def train_launches(shape, gather=False):
     """Kernels of one training step: the forward's, then combine backward,
     two Dgrad and two Wgrad GEMMs, the router backward's two kernels, and,
     when the forward gathered its rows, a permute and the recomputation of
-    the gate/up products."""
+    the gate/up products.  FP8 kind: the Dgrad quantises dy (one launch per
+    class: routed, shared), recomputes [a | b], forms dh, quantises
+    [da | db] and forms dx (four launches); the Wgrad pads the segment
+    starts, writes each of its four operands transposed in 128 x 1 tiles
+    (one launch per operand and class) and runs its two GEMMs."""
+    if shape.dtype == "fp8":
+        cls = 1 + (1 if shape.n_shared else 0)
+        return launches_per_step(shape) + 1 + (cls + 4) + 2 + (1 + 4 * cls + 2)
     return launches_per_step(shape, gather) + 1 + 2 + 2 + 2 + (2 if gather else 0)
 
 
@@ -359,6 +368,27 @@ def oracle_train_sample(shape, L, n_tokens, token0=0):
     ws13 = View(L["ws13"]) if shape.n_shared else None
     ws2 = View(L["ws2"]) if shape.n_shared else None
     t0 = time.perf_counter()
+    if shape.dtype == "fp8":
+        # FP8 forward, then each expert's FP8 Dgrad and Wgrad on its rows
+        # (dL/dy of a row = its gate times dL/d(out) of its token); the
+        # router's backward is not part of this sample
+        from oracle.moe_fp8 import moe_layer_forward_fp8
+        from oracle.moe_fp8_backward import fp8_swiglu_ffn_backward
+        fwd = moe_layer_forward_fp8(x, rw, b, View(L["w13"]), View(L["w2"]), ws13, ws2,
+                                    n_groups=shape.n_groups, topk_groups=shape.topk_groups,
+                                    k=shape.k, route_scale=shape.route_scale)
+        off, tor = fwd["offsets"], fwd["token_of_row"]
+        slot = np.argsort(fwd["row_of_slot"].reshape(-1))
+        gate_of_row = fwd["topk_w"].reshape(-1)[slot]
+        for e in range(shape.E):
+            lo, hi = int(off[e]), int(off[e + 1])
+            if hi > lo:
+                t = tor[lo:hi]
+                fp8_swiglu_ffn_backward(fwd["x_q"][t], fwd["x_scale"][t], View(L["w13"])[e],
+                                        View(L["w2"])[e], gate_of_row[lo:hi, None] * go[t])
+        for j in range(shape.n_shared):
+            fp8_swiglu_ffn_backward(fwd["x_q"], fwd["x_scale"], ws13[j], ws2[j], go)
+        return time.perf_counter() - t0, n_tokens
     fwd = oracle.moe_layer_forward(x, rw, b, View(L["w13"]), View(L["w2"]), ws13, ws2,
                                    n_groups=shape.n_groups, topk_groups=shape.topk_groups,
                                    k=shape.k, route_scale=shape.route_scale)
@@ -628,8 +658,11 @@ def run_train(args, shape, world, rank, local):
     import mixture_experts_layer_82_b300 as moe
     from moe_synth import make_grad
 
-    if shape.dtype != "bf16":
-        raise SystemExit("--train: the backward pass is implemented for the bf16 kind")
+    if shape.dtype not in ("bf16", "fp8"):
+        raise SystemExit("--train: the backward pass is implemented for the bf16 and fp8 kinds")
+    fp8 = shape.dtype == "fp8"
+    if fp8 and args.dispatch == "gather":
+        raise SystemExit("--train: the gathering forward is implemented for the bf16 kind")
     dev = f"cuda:{local}"
     torch.cuda.set_device(local)
     L = make_layer(shape, dev)
@@ -708,6 +741,12 @@ def run_train(args, shape, world, rank, local):
     peaks = load_peaks()
     peak = peaks["bf16_tflops"]
     peak_sust = peaks.get("bf16_tflops_sustained", peak)
+    peak_kind = f"bf16 dense burst, {peaks['_source']}"
+    if fp8:
+        # the measured bf16 peak times the nominal dense FP8 : bf16 ratio
+        # of B300 (4.5 : 2.25 PFLOP/s)
+        peak, peak_sust = 2.0 * peak, 2.0 * peak_sust
+        peak_kind = f"fp8 dense = 2 x bf16 dense burst, {peaks['_source']}"
     bf = backward_flops(shape)
     alg = {"forward experts": expert_flops(shape),
            "backward experts, input (Dgrad)": bf["dgrad"],
@@ -726,10 +765,14 @@ def run_train(args, shape, world, rank, local):
     line = {
         "metric": METRIC_TRAIN, "value": tokens / (total_ms * 1e-3), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype,
         "data": "synthetic",
         "config": {"workload": describe(shape), "global_batch": world * shape.T,
-                   "step": "forward (route, permute, experts keeping [a|b], combine, bias update) + "
+                   "step": "forward in FP8 (route, quantise + permute, experts, combine, bias "
+                           "update) + backward (combine, experts Dgrad in FP8 with [a|b] "
+                           "recomputed from the forward's codes, router, experts Wgrad in FP8)"
+                           if fp8 else
+                           "forward (route, permute, experts keeping [a|b], combine, bias update) + "
                            "backward (combine, experts Dgrad, router, experts Wgrad)"
                            if not gather else
                            "forward (route, experts gathering rows, combine, bias update) + backward "
@@ -741,10 +784,11 @@ def run_train(args, shape, world, rank, local):
         "layer_tflops": step_flops * world * K / (total_ms * 1e-3) / 1e12,
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_kind": f"bf16 dense burst, {peaks['_source']}",
+                     "peak_kind": peak_kind,
                      "frac_of_sustained": achieved / peak_sust, "traffic": None,
                      "breakdown": breakdown,
-                     "recompute_tflop_not_counted": bf["recompute"] / 1e12 if gather else 0.0},
+                     "recompute_tflop_not_counted":
+                         bf["recompute"] / 1e12 if (gather or fp8) else 0.0},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": dx_host.numel() * dx_host.element_size(),

@@ -161,11 +161,12 @@ def test_backward_workspace_formula_and_kinds():
     dgrad = (_align256(rows * d) + _align256(rows * (d // 128) * 4) + _align256(rows * 2 * I * 2)
              + _align256(rows * I * 2) + _align256(rows * 2 * I)
              + _align256(rows * (2 * I // 128) * 4))
-    # Wgrad: padded segment starts, then dy, u, h, [da | db] transposed with
-    # every segment padded to 128 rows (routed) and the shared expert's T rows
+    # Wgrad: padded segment starts and the rows of every padded tile, then
+    # the codes and scales of dy, u, h, [da | db] with every segment padded
+    # to 128 rows (routed) and the shared expert's T rows
     P = (tk + 127 * E + 127) // 128 * 128
     Ps = (T + 127) // 128 * 128
-    wgrad = _align256((E + 1) * 4) + sum(
+    wgrad = _align256((E + 1) * 4) + _align256(P // 128 * 8) + sum(
         _align256(C * P) + _align256(P // 128 * C * 4) + _align256(C * Ps)
         + _align256(Ps // 128 * C * 4) for C in (d, d, I, 2 * I))
     assert moe.moe_backward_workspace_bytes(f) == dgrad + wgrad + _align256(tk * 4)
