@@ -56,6 +56,13 @@ def test_training_launches_match_the_launch_list():
             == bench.train_launches(CONFIGS["v3_bf16"]) + 1)
 
 
+def test_fp8_training_launches_match_the_launch_list():
+    rows = _step_rows("launches_v3_fp8_train.md")
+    assert bench.train_launches(CONFIGS["v3_fp8"]) == len(rows)
+    assert sum("wgrad_fp8" in r for r in rows) == 2
+    assert sum("quant_rows" in r for r in rows) == 8   # 4 operands x (routed, shared)
+
+
 def test_algorithmic_flops():
     s = CONFIGS["v3_bf16"]
     rows = s.T * s.k + s.T * s.n_shared
