@@ -52,8 +52,20 @@ METRIC = "MoE-layer tokens/s at V3 shape (bf16, FP8); TFLOP/s as % of B300 peak"
 METRIC_TRAIN = ("MoE-layer training tokens/s (forward + backward) at V3 shape (bf16); "
                 "TFLOP/s as % of B300 peak")
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-KERNEL_SRC = {"bf16": "mixture_experts_layer_82_b300/csrc/experts_sm100.cu",
-              "fp8": "mixture_experts_layer_82_b300/csrc/experts_fp8.cu"}
+# sources of the expert GEMM kernels of each kind (the bf16 calls dispatch
+# between the pair-MMA and the multicast-pair kernels)
+KERNEL_SRC = {"bf16": ["mixture_experts_layer_82_b300/csrc/experts_sm100.cu",
+                       "mixture_experts_layer_82_b300/csrc/experts_pair.cu"],
+              "fp8": ["mixture_experts_layer_82_b300/csrc/experts_fp8.cu"]}
+
+
+def kernel_src_sha256(dtype):
+    """SHA-256 of the kind's kernel sources, concatenated in order."""
+    h = hashlib.sha256()
+    for f in KERNEL_SRC[dtype]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 # --------------------------------------------------------------- workload
@@ -153,11 +165,10 @@ def load_peaks():
 def kernel_traffic(dtype, workload):
     """DRAM bytes per launch of the expert GEMM pair from the committed ncu
     summary, if the kernel source has not changed since it was taken."""
-    src = os.path.join(ROOT, KERNEL_SRC.get(dtype, ""))
     summ = os.path.join(ROOT, "profiles", f"experts_{dtype}_{workload}_traffic.json")
-    if not (os.path.exists(src) and os.path.exists(summ)):
+    if dtype not in KERNEL_SRC or not os.path.exists(summ):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    sha = kernel_src_sha256(dtype)
     with open(summ) as f:
         d = json.load(f)
     if d.get("kernel_src_sha256") != sha:
@@ -597,8 +608,10 @@ def measure_ours(args, shape, world, rank, local, cpu_baseline):
     # this replica's loads (counts hold the summed loads when replicas > 1)
     ebytes, touched = expert_bytes(shape, np.diff(layer.offsets.cpu().numpy()))
     hbm_achieved = ebytes / (exp_mean * 1e-3) / 1e9
-    kernel = (f"experts_{shape.dtype}_kernel (gate/up + down launches of one "
-              f"moe_experts_grouped call)")
+    # the bf16 calls run pair MMAs when the segments average >= 128 rows
+    kname = (f"experts_{shape.dtype}_kernel" if shape.dtype != "bf16" or args.dispatch == "gather"
+             or shape.T * shape.k < 128 * shape.E else "experts_bf16_pair_kernel")
+    kernel = f"{kname} (gate/up + down launches of one moe_experts_grouped call)"
     traffic = kernel_traffic(shape.dtype, shape.name)
     if shape.T * shape.k < 16 * shape.E:  # fewer than 16 rows per expert on average
         # decode-sized batch: the expert GEMMs stream the touched weights

@@ -553,8 +553,8 @@ cudaError_t launch_experts_bwd_input_bf16(const ExpertsBwdArgs& a, cudaStream_t 
     g.offsets = a.offsets; g.n_rows = static_cast<int>(tk); g.E = c.E; g.T = c.T; g.has_shared = has_shared ? 1 : 0;
     g.d = 2 * I;   // B rows of one routed matrix
     g.inter = d;   // K of one matrix
-    // (each map also with half its box: the kernel runs in CTA pairs that
-    // split and share one operand of two tiles)
+    // (each map also with half its box: the pair kernel's CTAs hold half a
+    // B tile each, and 64 A rows each in a segment's last half tile)
     CUresult r = encode_bf16_2d(&g.a_map[0], a.x_perm, d, tk, BK, BM);
     if (r == CUDA_SUCCESS) r = encode_bf16_2d(&g.a_half[0], a.x_perm, d, tk, BK, BM / 2);
     if (r == CUDA_SUCCESS)
@@ -577,7 +577,7 @@ cudaError_t launch_experts_bwd_input_bf16(const ExpertsBwdArgs& a, cudaStream_t 
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     g.cls[0] = ClassDesc{w.ab, 2 * I, 2 * I, d};
     g.cls[1] = ClassDesc{w.ab_shared, Ns * 2 * I, Ns * 2 * I, d};
-    cudaError_t e = launch_bf16_gemm<DOWN, false>(g, st);
+    cudaError_t e = launch_bf16_pair_gemm<DOWN>(g, st);
     if (e != cudaSuccess) return e;
   }
 

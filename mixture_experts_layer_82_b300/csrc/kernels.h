@@ -224,11 +224,12 @@ CUresult encode_tensor_map_nd(CUtensorMap* m, CUtensorMapDataType dt, void* base
                               const uint32_t* box, CUtensorMapSwizzle swizzle);
 
 // The gate/up weights [n, 2I, d] seen as [n][2][I][d]: one box of
-// box_k x 128 x 2 x 1 is 128 W1 rows followed by the matching 128 W3 rows
-// (box_mats = 2); with box_mats = 1 a box is the 128 W1 or the 128 W3 rows.
+// box_k x box_rows x 2 x 1 is box_rows W1 rows followed by the matching
+// box_rows W3 rows (box_mats = 2); with box_mats = 1 a box is the W1 or the
+// W3 rows alone.
 CUresult encode_gate_up_map(CUtensorMap* m, CUtensorMapDataType dt, const void* w13, int n,
                             int inter, int d, size_t elem_bytes, uint32_t box_k,
-                            uint32_t box_mats = 2);
+                            uint32_t box_mats = 2, uint32_t box_rows = 128);
 
 // The gate/up weights [n, 2I, d] seen as [n][I/64][2][64][d]: one box of
 // box_k x 64 x 2 x 2 x 1 is 64 W1 rows, the matching 64 W3 rows, the next

@@ -38,12 +38,12 @@ CUresult encode_tensor_map_nd(CUtensorMap* m, CUtensorMapDataType dt, void* base
 
 CUresult encode_gate_up_map(CUtensorMap* m, CUtensorMapDataType dt, const void* w13, int n,
                             int inter, int d, size_t elem_bytes, uint32_t box_k,
-                            uint32_t box_mats) {
+                            uint32_t box_mats, uint32_t box_rows) {
   const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(inter), 2,
                             static_cast<uint64_t>(n)};
   const uint64_t row = static_cast<uint64_t>(d) * elem_bytes;
   const uint64_t strides[3] = {row, row * inter, row * inter * 2};
-  const uint32_t box[4] = {box_k, 128, box_mats, 1};
+  const uint32_t box[4] = {box_k, box_rows, box_mats, 1};
   return encode_tensor_map_nd(m, dt, const_cast<void*>(w13), 4, dims, strides, box,
                               CU_TENSOR_MAP_SWIZZLE_128B);
 }

@@ -309,7 +309,16 @@ def test_forward_into_a_given_output_buffer():
     # the smallest bf16 sizes: d = I = 128, no shared expert
     shape_with(CONFIGS["mid_bf16"], T=130, d=128, E=16, n_groups=4, topk_groups=2, k=4,
                n_shared=0, inter=128),
-], ids=lambda s: f"E{s.E}-d{s.d}-I{s.inter}-Ns{s.n_shared}")
+    # at least 128 rows per expert on average, so the GEMMs run as pair MMAs:
+    # the same half-outside last down tile and two shared experts, segments
+    # with whole 256-row pair tiles and a ragged second half, and half tiles
+    shape_with(CONFIGS["mid_bf16"], T=1024, d=640, E=8, n_groups=4, topk_groups=2, k=2,
+               n_shared=2, inter=384),
+    # pair MMAs at d = I = 128, one expert per token: half tiles whose second
+    # CTA holds some of the rows, none of them, or a full tile's ragged half
+    shape_with(CONFIGS["mid_bf16"], T=1400, d=128, E=4, n_groups=2, topk_groups=1, k=1,
+               n_shared=0, inter=128),
+], ids=lambda s: f"T{s.T}-E{s.E}-d{s.d}-I{s.inter}-Ns{s.n_shared}")
 def test_layer_edge_shapes(shape):
     L, cfg, layer = _layer(shape)
     aff = torch.empty(shape.T, shape.E, dtype=torch.float32, device=DEV)
