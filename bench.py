@@ -19,9 +19,8 @@ Rank 0 prints one JSON line.
 
 ``--train`` (bf16 and fp8 kinds) makes a step one training pass instead: the
 forward above, then its backward (combine backward, expert Dgrad, router
-backward, expert Wgrad), given a fixed dL/dy.  The bf16 forward keeps the
-gate/up products for the backward; the FP8 backward recomputes them from the
-forward's codes.
+backward, expert Wgrad), given a fixed dL/dy.  The forward keeps the
+gate/up products for the backward.
 
 ``--impl reference`` times the CPU oracle (fp64 NumPy) on the host cores on a
 bounded sample of the same workload; that is the only other place, besides
@@ -112,14 +111,14 @@ def train_launches(shape, gather=False):
     """Kernels of one training step: the forward's, then combine backward,
     two Dgrad and two Wgrad GEMMs, the router backward's two kernels, and,
     when the forward gathered its rows, a permute and the recomputation of
-    the gate/up products.  FP8 kind: the Dgrad quantises dy (one launch per
-    class: routed, shared), recomputes [a | b], forms dh, quantises
-    [da | db] and forms dx (four launches); the Wgrad pads the segment
+    the gate/up products.  FP8 kind (the forward keeps [a | b]): the Dgrad
+    quantises dy (one launch per class: routed, shared), forms dh,
+    quantises [da | db] and forms dx (three launches); the Wgrad pads the segment
     starts, writes each of its four operands transposed in 128 x 1 tiles
     (one launch per operand and class) and runs its two GEMMs."""
     if shape.dtype == "fp8":
         cls = 1 + (1 if shape.n_shared else 0)
-        return launches_per_step(shape) + 1 + (cls + 4) + 2 + (1 + 4 * cls + 2)
+        return launches_per_step(shape) + 1 + (cls + 3) + 2 + (1 + 4 * cls + 2)
     return launches_per_step(shape, gather) + 1 + 2 + 2 + 2 + (2 if gather else 0)
 
 
@@ -781,9 +780,9 @@ def run_train(args, shape, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype,
         "data": "synthetic",
         "config": {"workload": describe(shape), "global_batch": world * shape.T,
-                   "step": "forward in FP8 (route, quantise + permute, experts, combine, bias "
-                           "update) + backward (combine, experts Dgrad in FP8 with [a|b] "
-                           "recomputed from the forward's codes, router, experts Wgrad in FP8)"
+                   "step": "forward in FP8 (route, quantise + permute, experts keeping [a|b], "
+                           "combine, bias update) + backward (combine, experts Dgrad in FP8, "
+                           "router, experts Wgrad in FP8)"
                            if fp8 else
                            "forward (route, permute, experts keeping [a|b], combine, bias update) + "
                            "backward (combine, experts Dgrad, router, experts Wgrad)"
@@ -800,8 +799,7 @@ def run_train(args, shape, world, rank, local):
                      "peak_kind": peak_kind,
                      "frac_of_sustained": achieved / peak_sust, "traffic": None,
                      "breakdown": breakdown,
-                     "recompute_tflop_not_counted":
-                         bf["recompute"] / 1e12 if (gather or fp8) else 0.0},
+                     "recompute_tflop_not_counted": bf["recompute"] / 1e12 if gather else 0.0},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": dx_host.numel() * dx_host.element_size(),

@@ -458,6 +458,7 @@ moe_status_t moe_transpose_weights_fp8(const void* w_q, const float* w_scales,
  * tiles, 128 x 128 weight blocks).  The gradients are tiled along the
  * contraction of their GEMM, so that each tile's scale factors out:
  *   [a | b] = u W13^T   recomputed from the forward's E4M3 codes of u
+ *                       (unless moe_experts_grouped_train_fp8 kept it)
  *   dh = q(dy) W2       dy (bf16) in 1 x 128 tiles along d
  *   da = dh b silu'(a), db = dh silu(a)   in fp32
  *   du = q([da | db]) W13   [da | db] in 1 x 128 tiles along 2I
@@ -473,6 +474,8 @@ moe_status_t moe_transpose_weights_fp8(const void* w_q, const float* w_scales,
  *   dy_perm [T*K, d] bf16    from moe_combine_backward
  *   dout    [T, d] bf16      dL/dy of the layer (the shared expert's dy)
  *   dx_perm [T*K, d] bf16 out, dx_shared [T, d] bf16 out (NULL if N_s = 0)
+ *   ab_kept                  nonzero: `ws` holds [a | b] from this step's
+ *                            moe_experts_grouped_train_fp8 (not recomputed)
  *   ws, ws_bytes             at least moe_backward_workspace_bytes(cfg)
  * FP8 kind with at most one shared expert (MOE_ERR_SHAPE otherwise).  It
  * leaves [a | b] and dh in `ws` for moe_experts_backward_weights_fp8.
@@ -483,7 +486,27 @@ moe_status_t moe_experts_backward_input_fp8(
     const void* w13t, const float* w13t_scales, const void* w2t, const float* w2t_scales,
     const void* ws13, const float* ws13_scales, const void* ws13t, const float* ws13t_scales,
     const void* ws2t, const float* ws2t_scales, const void* dy_perm, const void* dout,
-    void* dx_perm, void* dx_shared, void* ws, size_t ws_bytes, void* stream);
+    void* dx_perm, void* dx_shared, int32_t ab_kept, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_experts_grouped_train_fp8 - moe_experts_grouped (FP8 kind, at most one
+ * shared expert) for a training step: the same outputs, and the gate/up
+ * epilogue also keeps a = x W1^T and b = x W3^T (the promoted fp32 sums,
+ * rounded to bf16) of every routed row and of the shared expert in the
+ * backward workspace `bws`, so that moe_experts_backward_input_fp8 with
+ * ab_kept = 1 does not recompute them (0.5 GB written at the DeepSeek-V3
+ * shape instead of 4.3 TFLOP of FP8 GEMM).
+ *   arguments as in moe_experts_grouped, plus
+ *   bws, bws_bytes   at least moe_backward_workspace_bytes(cfg); pass the
+ *                    same buffer to this step's backward calls
+ * MOE_ERR_SHAPE for another kind or more than one shared expert.
+ */
+moe_status_t moe_experts_grouped_train_fp8(
+    const moe_cfg_t* cfg, const void* x_perm, const float* x_perm_scales, const void* x,
+    const float* x_scales, const int32_t* offsets, const void* w13, const float* w13_scales,
+    const void* w2, const float* w2_scales, const void* ws13, const float* ws13_scales,
+    const void* ws2, const float* ws2_scales, void* y_perm, void* y_shared, void* ws,
+    size_t ws_bytes, void* bws, size_t bws_bytes, void* stream);
 
 /*
  * moe_experts_backward_weights_fp8 - Wgrad of every expert FFN in FP8 E4M3

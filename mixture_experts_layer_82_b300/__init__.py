@@ -43,7 +43,8 @@ EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_byt
             "moe_selftest_wait", "moe_backward_workspace_bytes", "moe_combine_backward",
             "moe_experts_backward_input", "moe_experts_backward_weights", "moe_route_backward",
             "moe_experts_grouped_train", "moe_experts_grouped_gated", "moe_transpose_weights_fp8",
-            "moe_experts_backward_input_fp8", "moe_experts_backward_weights_fp8")
+            "moe_experts_backward_input_fp8", "moe_experts_backward_weights_fp8",
+            "moe_experts_grouped_train_fp8")
 
 
 class MoeCfg(ctypes.Structure):
@@ -113,7 +114,11 @@ _lib.moe_transpose_weights_fp8.restype = ctypes.c_int
 _lib.moe_transpose_weights_fp8.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                            _P, _P, _P]
 _lib.moe_experts_backward_input_fp8.restype = ctypes.c_int
-_lib.moe_experts_backward_input_fp8.argtypes = [_CFG] + [_P] * 21 + [_P, ctypes.c_size_t, _P]
+_lib.moe_experts_backward_input_fp8.argtypes = ([_CFG] + [_P] * 21 +
+                                                [ctypes.c_int32, _P, ctypes.c_size_t, _P])
+_lib.moe_experts_grouped_train_fp8.restype = ctypes.c_int
+_lib.moe_experts_grouped_train_fp8.argtypes = ([_CFG] + [_P] * 16 +
+                                               [ctypes.c_size_t, _P, ctypes.c_size_t, _P])
 _lib.moe_experts_backward_weights_fp8.restype = ctypes.c_int
 _lib.moe_experts_backward_weights_fp8.argtypes = [_CFG] + [_P] * 11 + [_P, ctypes.c_size_t, _P]
 
@@ -410,9 +415,10 @@ def moe_transpose_weights_fp8(q, scales, qt, scales_t, stream=None):
 def moe_experts_backward_input_fp8(cfg, x_perm, x_perm_scales, x_q, x_q_scales, offsets, w13,
                                    w13_scales, w13t, w13t_scales, w2t, w2t_scales, ws13,
                                    ws13_scales, ws13t, ws13t_scales, ws2t, ws2t_scales, dy_perm,
-                                   dout, dx_perm, dx_shared, ws, stream=None):
+                                   dout, dx_perm, dx_shared, ws, ab_kept=False, stream=None):
     """Dgrad of every expert FFN in FP8 (gradients in 1 x 128 tiles along
-    their GEMM's contraction, weights in their forward blocks)."""
+    their GEMM's contraction, weights in their forward blocks).
+    ab_kept: ws holds [a | b] from this step's moe_experts_grouped_train_fp8."""
     opt = dict(allow_none=True)
     _check("moe_experts_backward_input_fp8", _lib.moe_experts_backward_input_fp8(
         _cfg(cfg), _ptr(x_perm, "x_perm", _F8), _ptr(x_perm_scales, "x_perm_scales", torch.float32),
@@ -426,7 +432,26 @@ def moe_experts_backward_input_fp8(cfg, x_perm, x_perm_scales, x_q, x_q_scales, 
         _ptr(ws2t, "ws2t", _F8, **opt), _ptr(ws2t_scales, "ws2t_scales", torch.float32, **opt),
         _ptr(dy_perm, "dy_perm", _BF), _ptr(dout, "dout", _BF, **opt),
         _ptr(dx_perm, "dx_perm", _BF), _ptr(dx_shared, "dx_shared", _BF, **opt),
-        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+        1 if ab_kept else 0, _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_experts_grouped_train_fp8(cfg, x_perm, x_perm_scales, x, x_scales, offsets, w13,
+                                  w13_scales, w2, w2_scales, ws13, ws13_scales, ws2, ws2_scales,
+                                  y_perm, y_shared, ws, bws, stream=None):
+    """moe_experts_grouped (FP8) that also keeps [a | b] in the backward
+    workspace bws for moe_experts_backward_input_fp8(..., ab_kept=True)."""
+    opt = dict(allow_none=True)
+    _check("moe_experts_grouped_train_fp8", _lib.moe_experts_grouped_train_fp8(
+        _cfg(cfg), _ptr(x_perm, "x_perm", _F8), _ptr(x_perm_scales, "x_perm_scales", torch.float32),
+        _ptr(x, "x", _F8, **opt), _ptr(x_scales, "x_scales", torch.float32, **opt),
+        _ptr(offsets, "offsets", torch.int32),
+        _ptr(w13, "w13", _F8), _ptr(w13_scales, "w13_scales", torch.float32),
+        _ptr(w2, "w2", _F8), _ptr(w2_scales, "w2_scales", torch.float32),
+        _ptr(ws13, "ws13", _F8, **opt), _ptr(ws13_scales, "ws13_scales", torch.float32, **opt),
+        _ptr(ws2, "ws2", _F8, **opt), _ptr(ws2_scales, "ws2_scales", torch.float32, **opt),
+        _ptr(y_perm, "y_perm", _BF), _ptr(y_shared, "y_shared", _BF, **opt),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(),
+        _ptr(bws, "bws"), bws.numel() * bws.element_size(), _stream(stream)))
 
 
 def moe_experts_backward_weights_fp8(cfg, x_perm, x_perm_scales, x_q, x_q_scales, offsets,

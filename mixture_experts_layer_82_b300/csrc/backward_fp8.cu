@@ -257,11 +257,14 @@ cudaError_t launch_experts_bwd_input_fp8(const ExpertsBwdFp8Args& a, cudaStream_
   if (e == cudaSuccess && has_shared)
     e = launch_quantize_act_fp8(a.dout, c.T, d, dyq_sh, dys_sh, st);
   if (e != cudaSuccess) return e;
-  // 2. [a | b] = u W13^T from the forward's codes
+  // 2. [a | b] = u W13^T from the forward's codes (unless the training
+  //    forward kept it)
   Fp8Gemm g{a.x_perm, a.x_perm_scales, a.x_q, a.x_q_scales, a.w13, a.w13_scales,
             a.ws13, a.ws13_scales, s.ab, ab_sh, 2 * I, d};
-  e = run_fp8_gemm(c, a.offsets, g, st);
-  if (e != cudaSuccess) return e;
+  if (!a.ab_kept) {
+    e = run_fp8_gemm(c, a.offsets, g, st);
+    if (e != cudaSuccess) return e;
+  }
   // 3. dh = q(dy) W2, through W2^T [I, d]
   g = Fp8Gemm{s.dyq, s.dys, dyq_sh, dys_sh, a.w2t, a.w2t_scales, a.ws2t, a.ws2t_scales,
               s.dh, dh_sh, I, d};

@@ -81,6 +81,7 @@ struct ClassDesc {
   int n_out;              // output columns (row stride of out)
   int k_dim;              // reduction length
   const float* gate;      // down, optional: every output row is multiplied by gate[row]
+  __nv_bfloat16* ab;      // gate/up, optional: [a | b] rows [rows, 2I] kept for the backward
 };
 
 struct Params {
@@ -310,7 +311,9 @@ __device__ __forceinline__ bool promote_block(Smem& s, float (&acc)[128], uint32
   return true;
 }
 
-template <int MODE>
+// KEEP_AB (gate/up of a training forward): also store a and b in bf16; a
+// separate instantiation, since the stores cost the epilogue registers.
+template <int MODE, bool KEEP_AB = false>
 __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
@@ -512,6 +515,23 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
       const bool valid = m < tl.rows;
       const size_t grow = static_cast<size_t>(tl.row0) + (valid ? m : 0);
       if (MODE == GATEUP) {
+        // training forward: a and b of this row's 64 h columns, kept in bf16
+        // for the backward at [a | b] (I columns each)
+        if (KEEP_AB && cd.ab != nullptr && valid) {
+          __nv_bfloat16* arow = cd.ab + grow * (2 * static_cast<size_t>(p.inter)) +
+                                tl.nt * (BN / 2) + hf * 64;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            reinterpret_cast<uint4*>(arow)[c] =
+                make_uint4(pack_bf16x2(acc[8 * c], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
+                           pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+            reinterpret_cast<uint4*>(arow + p.inter)[c] =
+                make_uint4(pack_bf16x2(acc[64 + 8 * c], acc[64 + 8 * c + 1]),
+                           pack_bf16x2(acc[64 + 8 * c + 2], acc[64 + 8 * c + 3]),
+                           pack_bf16x2(acc[64 + 8 * c + 4], acc[64 + 8 * c + 5]),
+                           pack_bf16x2(acc[64 + 8 * c + 6], acc[64 + 8 * c + 7]));
+          }
+        }
         // h = silu(a) * b, then one E4M3 scale per row and 128 h columns
         float amax = 0.f;
 #pragma unroll
@@ -584,13 +604,13 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
 
 }  // namespace fp8gemm
 
-template <int MODE>
+template <int MODE, bool KEEP_AB = false>
 static cudaError_t launch_fp8_gemm(const fp8gemm::Params& prm, cudaStream_t st) {
   using namespace fp8gemm;
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(experts_fp8_kernel<MODE>),
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(experts_fp8_kernel<MODE, KEEP_AB>),
                                     static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  experts_fp8_kernel<MODE><<<sm_count(), THREADS, kSmemBytes, st>>>(prm);
+  experts_fp8_kernel<MODE, KEEP_AB><<<sm_count(), THREADS, kSmemBytes, st>>>(prm);
   return cudaGetLastError();
 }
 
@@ -627,10 +647,11 @@ cudaError_t launch_experts_fp8(const ExpertsArgs& a, cudaStream_t st) {
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const auto al32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
   g.out32 = al32(h_routed) && al32(h_shared) ? 1 : 0;
-  g.cls[0] = ClassDesc{h_routed, hs_routed, a.x_perm_scales, a.w13_scales, I, c.d};
+  g.cls[0] = ClassDesc{h_routed, hs_routed, a.x_perm_scales, a.w13_scales, I, c.d, nullptr, a.ab};
   g.cls[1] = ClassDesc{h_shared, hs_shared, has_shared ? a.x_scales : a.x_perm_scales,
-                       has_shared ? a.ws13_scales : a.w13_scales, Ns * I, c.d};
-  cudaError_t e = launch_fp8_gemm<GATEUP>(g, st);
+                       has_shared ? a.ws13_scales : a.w13_scales, Ns * I, c.d, nullptr,
+                       has_shared ? a.ab_shared : nullptr};
+  cudaError_t e = a.ab != nullptr ? launch_fp8_gemm<GATEUP, true>(g, st) : launch_fp8_gemm<GATEUP>(g, st);
   if (e != cudaSuccess) return e;
 
   // ---- down: A = h codes, B = W2 (E4M3)

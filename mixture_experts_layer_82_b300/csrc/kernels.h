@@ -84,8 +84,8 @@ struct ExpertsArgs {
   const int32_t* token_of_row;  // non-null: gate/up gathers its routed A rows from x
   void* h;            // workspace: routed rows [T*K, I] then shared rows [T, Ns*I]
   float* h_scales;    // FP8: [T*K, I/128] then [T, Ns*I/128]
-  __nv_bfloat16* ab;         // bf16 training forward, optional: [a | b] rows kept for
-  __nv_bfloat16* ab_shared;  // the backward ([T*K, 2I] and [T, Ns*2I])
+  __nv_bfloat16* ab;         // training forward, optional: [a | b] rows kept for the
+  __nv_bfloat16* ab_shared;  // backward ([T*K, 2I] and [T, Ns*2I]; FP8: Ns <= 1)
   const float* gate_of_row;  // optional [T*K]: the down projection writes gate * y
 };
 
@@ -152,6 +152,7 @@ struct ExpertsBwdFp8Args {
   void* dx_perm;               // [T*K, d] bf16 out
   void* dx_shared;             // [T, d] bf16 out
   void* ws;                    // experts_bwd_fp8_scratch_bytes
+  bool ab_kept;                // ws already holds [a | b] from the training forward
 };
 size_t experts_bwd_fp8_scratch_bytes(const moe_cfg_t& c);
 

@@ -160,7 +160,9 @@ static moe_status_t experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
                                     const float* ws13_scales, const void* ws2,
                                     const float* ws2_scales, const int32_t* row_of_slot,
                                     const float* topk_w, void* y_perm, void* y_shared, void* ws,
-                                    size_t ws_bytes, void* stream) {
+                                    size_t ws_bytes, void* stream,
+                                    __nv_bfloat16* ab = nullptr,
+                                    __nv_bfloat16* ab_shared = nullptr) {
   moe_status_t st = moe_check_cfg(cfg);
   if (st != MOE_OK) return st;
   const moe_cfg_t& c = *cfg;
@@ -187,6 +189,8 @@ static moe_status_t experts_grouped(const moe_cfg_t* cfg, const void* x_perm,
   a.w13 = w13; a.w13_scales = w13_scales; a.w2 = w2; a.w2_scales = w2_scales;
   a.ws13 = ws13; a.ws13_scales = ws13_scales; a.ws2 = ws2; a.ws2_scales = ws2_scales;
   a.y_perm = y_perm; a.y_shared = c.n_shared > 0 ? y_shared : nullptr;
+  a.ab = ab;
+  a.ab_shared = c.n_shared > 0 ? ab_shared : nullptr;
   experts_scratch_carve(c, ws, &a.h, &a.h_scales);
   cudaStream_t s = as_stream(stream);
   cudaError_t e;
@@ -503,7 +507,7 @@ moe_status_t moe_experts_backward_input_fp8(
     const void* w13t, const float* w13t_scales, const void* w2t, const float* w2t_scales,
     const void* ws13, const float* ws13_scales, const void* ws13t, const float* ws13t_scales,
     const void* ws2t, const float* ws2t_scales, const void* dy_perm, const void* dout,
-    void* dx_perm, void* dx_shared, void* ws, size_t ws_bytes, void* stream) {
+    void* dx_perm, void* dx_shared, int32_t ab_kept, void* ws, size_t ws_bytes, void* stream) {
   moe_status_t st = moe_check_cfg(cfg);
   if (st != MOE_OK) return st;
   const moe_cfg_t& c = *cfg;
@@ -536,7 +540,30 @@ moe_status_t moe_experts_backward_input_fp8(
   a.dy_perm = dy_perm; a.dout = dout; a.dx_perm = dx_perm;
   a.dx_shared = c.n_shared > 0 ? dx_shared : nullptr;
   a.ws = ws;
+  a.ab_kept = ab_kept != 0;
   return from_cuda(launch_experts_bwd_input_fp8(a, as_stream(stream)));
+}
+
+moe_status_t moe_experts_grouped_train_fp8(
+    const moe_cfg_t* cfg, const void* x_perm, const float* x_perm_scales, const void* x,
+    const float* x_scales, const int32_t* offsets, const void* w13, const float* w13_scales,
+    const void* w2, const float* w2_scales, const void* ws13, const float* ws13_scales,
+    const void* ws2, const float* ws2_scales, void* y_perm, void* y_shared, void* ws,
+    size_t ws_bytes, void* bws, size_t bws_bytes, void* stream) {
+  moe_status_t st = moe_check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_cfg_t& c = *cfg;
+  if (c.dtype != MOE_DTYPE_FP8_E4M3 || c.n_shared > 1) return MOE_ERR_SHAPE;
+  if (bws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(bws)) return MOE_ERR_ALIGN;
+  if (bws_bytes < moe_backward_workspace_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  const __nv_bfloat16 *ab = nullptr, *dh = nullptr;
+  experts_bwd_fp8_ab_dh(c, bws, &ab, &dh);
+  __nv_bfloat16* abw = const_cast<__nv_bfloat16*>(ab);
+  return experts_grouped(cfg, x_perm, x_perm_scales, x, x_scales, offsets, w13, w13_scales, w2,
+                         w2_scales, ws13, ws13_scales, ws2, ws2_scales, nullptr, nullptr, y_perm,
+                         y_shared, ws, ws_bytes, stream, abw,
+                         abw + static_cast<size_t>(c.T) * c.K * 2 * c.inter);
 }
 
 moe_status_t moe_experts_backward_weights_fp8(

@@ -14,7 +14,7 @@ from . import (LayerCfg, moe_route, moe_permute, moe_experts_grouped, moe_expert
                moe_backward_workspace_bytes, moe_combine_backward, moe_experts_backward_input,
                moe_experts_backward_weights, moe_route_backward, moe_experts_grouped_train,
                moe_transpose_weights_fp8, moe_experts_backward_input_fp8,
-               moe_experts_backward_weights_fp8)
+               moe_experts_backward_weights_fp8, moe_experts_grouped_train_fp8)
 
 
 def _transpose_fp8(q, s, stream=None):
@@ -90,8 +90,8 @@ class MoELayer:
         ``stream`` around the grouped expert GEMMs, for timing them inside a
         step.  ``gather`` (default: ``self.gather``) folds the permute into
         the gate/up GEMM (moe_experts_grouped_gather; bf16 kind).  ``keep``
-        (bf16 kind, permuting forward): keep the gate/up products for the
-        next ``backward`` instead of having it recompute them.
+        (bf16 and fp8 kinds, permuting forward): keep the gate/up products
+        for the next ``backward`` instead of having it recompute them.
         ``load_group``: a torch.distributed group of data-parallel replicas;
         the bias update then uses the whole batch's per-expert loads (one
         all-reduce of ``counts``, which afterwards hold the global loads).
@@ -102,7 +102,7 @@ class MoELayer:
         c = self.cfg
         out = self.out if out is None else out
         gather = self.gather if gather is None else gather
-        keep = keep and c.dtype == "bf16" and not gather
+        keep = keep and c.dtype in ("bf16", "fp8") and not gather
         gated = gated and not gather and not keep
         if keep and not hasattr(self, "bws"):
             self._grad_buffers()
@@ -122,7 +122,14 @@ class MoELayer:
             shared_in = self.x_q if c.dtype == "fp8" else x
             if expert_events is not None:
                 expert_events[0].record(stream)
-            if keep:
+            if keep and c.dtype == "fp8":
+                moe_experts_grouped_train_fp8(c, self.x_perm, self.x_perm_s, self.x_q, self.x_q_s,
+                                              self.offsets, self.w13, self.w13_s, self.w2,
+                                              self.w2_s, self.ws13, self.ws13_s, self.ws2,
+                                              self.ws2_s, self.y_perm, self.y_shared, self.ws,
+                                              self.bws, stream=stream)
+                self._ab_kept = True
+            elif keep:
                 moe_experts_grouped_train(c, self.x_perm, x, self.offsets, self.w13, self.w2,
                                           self.ws13, self.ws2, self.y_perm, self.y_shared, self.ws,
                                           self.bws, stream=stream)
@@ -211,7 +218,9 @@ class MoELayer:
                 c, self.x_perm, self.x_perm_s, self.x_q, self.x_q_s, self.offsets, self.w13,
                 self.w13_s, self.w13t, self.w13t_s, self.w2t, self.w2t_s, self.ws13, self.ws13_s,
                 self.ws13t, self.ws13t_s, self.ws2t, self.ws2t_s, self.dy_perm, dout,
-                self.dx_perm, self.dx_shared, self.bws, stream=stream)
+                self.dx_perm, self.dx_shared, self.bws,
+                ab_kept=getattr(self, "_ab_kept", False), stream=stream)
+            self._ab_kept = False  # a later backward without a new forward recomputes it
             if events is not None:
                 events[1].record(stream)
             moe_route_backward(c, x, self.router_w, affinity, self.topk_idx, self.dgate,

@@ -60,9 +60,11 @@ SHAPES = [
 ]
 
 
-def _run(shape, never=()):
+def _run(shape, never=(), keep=True):
     """Forward then backward of the FP8 layer; the experts in ``never`` get
-    a bias that keeps every token away from them (empty segments)."""
+    a bias that keeps every token away from them (empty segments).  ``keep``:
+    the training forward keeps [a | b] (moe_experts_grouped_train_fp8);
+    otherwise the Dgrad recomputes it from the codes."""
     L = make_layer(shape, DEV)
     cfg = moe.LayerCfg.from_shape(shape)
     bias = L["bias"].clone()
@@ -72,7 +74,7 @@ def _run(shape, never=()):
                          L["ws13"] if shape.n_shared else None,
                          L["ws2"] if shape.n_shared else None)
     aff = torch.empty(shape.T, shape.E, dtype=torch.float32, device=DEV)
-    layer.forward(L["x"], affinity_out=aff, update_bias=False)
+    layer.forward(L["x"], affinity_out=aff, update_bias=False, keep=keep)
     dout = make_grad(shape, DEV)
     dx = layer.backward(L["x"], dout, aff)
     assert moe.moe_get_device_error() == 0
@@ -212,6 +214,20 @@ def test_fp8_backward_is_deterministic():
     for u, v in ((w13, layer.dw13), (w2, layer.dw2), (ws13, layer.dws13)):
         assert torch.equal(u.view(torch.int16), v.view(torch.int16))
     assert moe.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("shape", [SHAPES[0], SHAPES[2]],
+                         ids=lambda s: f"T{s.T}-d{s.d}-E{s.E}-I{s.inter}-Ns{s.n_shared}")
+def test_fp8_kept_ab_matches_recomputed(shape):
+    """The training forward's [a | b] (the gate/up promotion's fp32 sums,
+    rounded to bf16) against the Dgrad's recompute from the same codes (the
+    same per-128-K promotion in the plain GEMM): the backward's outputs
+    agree far inside the FP8 bound."""
+    L, kept, dout, _ = _run(shape, keep=True)
+    got = [host(t).copy() for t in (kept.dx_perm, kept.dw13, kept.dw2)]
+    _, again, _, _ = _run(shape, keep=False)
+    for g, r, name in zip(got, (again.dx_perm, again.dw13, again.dw2), ("dx_perm", "dw13", "dw2")):
+        assert rel_frobenius(g, host(r)) < 2e-3, (name, rel_frobenius(g, host(r)))
 
 
 def test_fp8_weight_transpose_is_exact():
