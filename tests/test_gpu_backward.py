@@ -58,6 +58,10 @@ SHAPES = [
                n_shared=0, inter=128),
     # the mid-size workload's own widths on fewer tokens
     shape_with(CONFIGS["mid_bf16"], T=256),
+    # 256 rows per expert: the forward (keeping [a | b]) and the recompute run
+    # as pair MMAs; N tiles half outside I and d, two shared experts
+    shape_with(CONFIGS["mid_bf16"], T=1024, d=640, E=8, n_groups=4, topk_groups=2, k=2,
+               n_shared=2, inter=384),
 ]
 
 
@@ -105,12 +109,13 @@ def test_backward_is_deterministic():
         assert torch.equal(getattr(layer, k).view(bits), v.view(bits)), k
 
 
-def test_kept_gate_up_products_match_recomputed():
+@pytest.mark.parametrize("shape", [SHAPES[1], SHAPES[4]], ids=["multicast", "pair"])
+def test_kept_gate_up_products_match_recomputed(shape):
     """moe_experts_grouped_train keeps [a | b] from the forward's gate/up
     epilogue; the backward that uses them matches the one that recomputes
     them, and the training forward's own outputs equal the plain forward's
-    bit for bit."""
-    shape = SHAPES[1]
+    bit for bit (both GEMM kernels: fewer and more than 128 rows per
+    expert)."""
     L, layer = _layer(shape)
     _run(shape, L, layer, keep=False)
     ref = {k: getattr(layer, k).clone() for k in
