@@ -452,6 +452,24 @@ moe_status_t moe_transpose_weights_fp8(const void* w_q, const float* w_scales,
                                        void* wt_q, float* wt_scales, void* stream);
 
 /*
+ * moe_quantize_act_fp8_128x1 - E4M3 quantisation of bf16 x [rows, cols] in
+ * 128 x 1 tiles (128 consecutive rows of one column), the tiles Wgrad's
+ * operands use (moe_experts_backward_weights_fp8 quantises dy, u, h and
+ * [da | db] this way, per segment):
+ *   scale[t][c] = fl32(amax / 448) over rows 128t .. 128t + 127 of column c
+ *                 (1 for an all-zero tile; a ragged last tile over the rows
+ *                 it has)
+ *   q[r][c]     = E4M3(fl32(x[r][c] / scale)), nearest even, saturating
+ *   x       [rows, cols] bf16, cols % 128 == 0
+ *   q       [ceil(rows/128) * 128, cols] E4M3 out (the rows past `rows` of the
+ *           last tile are written as zero codes)
+ *   scales  [ceil(rows/128), cols] fp32 out
+ * MOE_ERR_SHAPE when cols is not a multiple of 128.
+ */
+moe_status_t moe_quantize_act_fp8_128x1(const void* x, int32_t rows, int32_t cols, void* q,
+                                        float* scales, void* stream);
+
+/*
  * moe_experts_backward_input_fp8 - Dgrad of every expert FFN in FP8 E4M3
  * (mixed precision framework paragraph, Figure 6: Dgrad in FP8 with fp32
  * accumulation; fine-grained quantisation paragraph: 1 x 128 activation

@@ -44,7 +44,7 @@ EXPORTED = ("moe_status_str", "moe_version", "moe_check_cfg", "moe_workspace_byt
             "moe_experts_backward_input", "moe_experts_backward_weights", "moe_route_backward",
             "moe_experts_grouped_train", "moe_experts_grouped_gated", "moe_transpose_weights_fp8",
             "moe_experts_backward_input_fp8", "moe_experts_backward_weights_fp8",
-            "moe_experts_grouped_train_fp8")
+            "moe_experts_grouped_train_fp8", "moe_quantize_act_fp8_128x1")
 
 
 class MoeCfg(ctypes.Structure):
@@ -116,6 +116,8 @@ _lib.moe_transpose_weights_fp8.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int3
 _lib.moe_experts_backward_input_fp8.restype = ctypes.c_int
 _lib.moe_experts_backward_input_fp8.argtypes = ([_CFG] + [_P] * 21 +
                                                 [ctypes.c_int32, _P, ctypes.c_size_t, _P])
+_lib.moe_quantize_act_fp8_128x1.restype = ctypes.c_int
+_lib.moe_quantize_act_fp8_128x1.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P]
 _lib.moe_experts_grouped_train_fp8.restype = ctypes.c_int
 _lib.moe_experts_grouped_train_fp8.argtypes = ([_CFG] + [_P] * 16 +
                                                [ctypes.c_size_t, _P, ctypes.c_size_t, _P])
@@ -433,6 +435,15 @@ def moe_experts_backward_input_fp8(cfg, x_perm, x_perm_scales, x_q, x_q_scales, 
         _ptr(dy_perm, "dy_perm", _BF), _ptr(dout, "dout", _BF, **opt),
         _ptr(dx_perm, "dx_perm", _BF), _ptr(dx_shared, "dx_shared", _BF, **opt),
         1 if ab_kept else 0, _ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_quantize_act_fp8_128x1(x, q, scales, stream=None):
+    """bf16 x [rows, cols] in 128 x 1 E4M3 tiles: codes q [ceil(rows/128)*128,
+    cols] (float8_e4m3fn) and fp32 scales [ceil(rows/128), cols]."""
+    rows, cols = x.shape
+    _check("moe_quantize_act_fp8_128x1", _lib.moe_quantize_act_fp8_128x1(
+        _ptr(x, "x", _BF), rows, cols, _ptr(q, "q", _F8), _ptr(scales, "scales", torch.float32),
+        _stream(stream)))
 
 
 def moe_experts_grouped_train_fp8(cfg, x_perm, x_perm_scales, x, x_scales, offsets, w13,

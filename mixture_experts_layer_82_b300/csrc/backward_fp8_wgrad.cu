@@ -148,6 +148,26 @@ __device__ __forceinline__ float4 staged_quad(const uint8_t* t, int r, int l, bo
                      h.w * (av.w * sg.w));
 }
 
+// E4M3 codes of fl32(a / sa) and fl32(b / sb) (nearest even, saturating),
+// given ra = fl32(1 / sa) and rb = fl32(1 / sb).  q = fl32(a ra) is within
+// 2.5 fp32 ulps of fl32(a / sa): ra carries half an ulp of relative error
+// and the product another half, and the quotient itself is rounded by half
+// an ulp.  The conversion to E4M3 is monotonic, so when q widened by 4 ulps
+// either way gives the same code, that is the code of fl32(a / sa); only a
+// quotient near an E4M3 rounding boundary takes the exact division.
+__device__ __forceinline__ uint32_t e4m3x2_of_quotients(float a, float b, float sa, float sb,
+                                                        float ra, float rb) {
+  const float qa = a * ra, qb = b * rb;
+  const float ea = fabsf(qa) * 0x1p-21f, eb = fabsf(qb) * 0x1p-21f;
+  const __nv_fp8x2_storage_t lo =
+      __nv_cvt_float2_to_fp8x2(make_float2(qa - ea, qb - eb), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi =
+      __nv_cvt_float2_to_fp8x2(make_float2(qa + ea, qb + eb), __NV_SATFINITE, __NV_E4M3);
+  if (lo == hi) return lo;
+  return __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, sa), __fdiv_rn(b, sb)), __NV_SATFINITE,
+                                  __NV_E4M3);
+}
+
 // One block per (128-row tile of the padded layout, 128 columns).  Thread
 // 0 copies the tile's source boxes into shared memory (rows past the
 // segment are copied too and zeroed here); warp w then forms rows
@@ -225,16 +245,14 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __grid_constant__
   }
   const float4 sc = make_float4(fp8_scale_of(m.x), fp8_scale_of(m.y), fp8_scale_of(m.z),
                                 fp8_scale_of(m.w));
+  const float4 rc = make_float4(__frcp_rn(sc.x), __frcp_rn(sc.y), __frcp_rn(sc.z), __frcp_rn(sc.w));
   const int c = c0 + 4 * lane;
   uint8_t* dst = a.q + static_cast<int64_t>(p0 + warp * 16) * a.C + c;
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
-    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-        make_float2(__fdiv_rn(v[r].x, sc.x), __fdiv_rn(v[r].y, sc.y)), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-        make_float2(__fdiv_rn(v[r].z, sc.z), __fdiv_rn(v[r].w, sc.w)), __NV_SATFINITE, __NV_E4M3);
-    *reinterpret_cast<uint32_t*>(dst + static_cast<int64_t>(r) * a.C) =
-        static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    const uint32_t lo = e4m3x2_of_quotients(v[r].x, v[r].y, sc.x, sc.y, rc.x, rc.y);
+    const uint32_t hi = e4m3x2_of_quotients(v[r].z, v[r].w, sc.z, sc.w, rc.z, rc.w);
+    *reinterpret_cast<uint32_t*>(dst + static_cast<int64_t>(r) * a.C) = lo | (hi << 16);
   }
   if (warp == 0) *reinterpret_cast<float4*>(a.s + static_cast<int64_t>(pt) * a.C + c) = sc;
 }
@@ -649,6 +667,22 @@ cudaError_t quantise_operand(const ExpertsBwdWeightsFp8Args& a, const WgScratch&
 }
 
 }  // namespace wgfp8
+
+cudaError_t launch_quantize_act_128x1(const void* x, int rows, int cols, uint8_t* q, float* scales,
+                                      cudaStream_t st) {
+  using namespace wgfp8;
+  QtParams prm{};
+  prm.tile_rows = nullptr;  // one segment: all rows
+  prm.n_rows = rows;
+  prm.C = cols;
+  CUresult r = encode_tensor_map_2d(&prm.src, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(x),
+                                    static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                                    static_cast<uint64_t>(cols) * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  prm.q = q;
+  prm.s = scales;
+  return launch_quant_rows<DY>(prm, dim3(static_cast<unsigned>((rows + 127) / 128), cols / 128), st);
+}
 
 size_t experts_wgrad_fp8_scratch_bytes(const moe_cfg_t& c) {
   return wgfp8::wg_bytes(c, nullptr, nullptr);

@@ -177,6 +177,10 @@ struct ExpertsBwdWeightsFp8Args {
   void* wg_ws;              // experts_wgrad_fp8_scratch_bytes
 };
 size_t experts_wgrad_fp8_scratch_bytes(const moe_cfg_t& c);
+// bf16 x [rows, cols] (cols % 128 == 0) in 128 x 1 tiles along the rows:
+// codes [round128(rows), cols] (rows past `rows` zero), scales [rows/128 up, cols].
+cudaError_t launch_quantize_act_128x1(const void* x, int rows, int cols, uint8_t* q, float* scales,
+                                      cudaStream_t s);
 cudaError_t launch_experts_bwd_weights_fp8(const ExpertsBwdWeightsFp8Args& a, cudaStream_t s);
 // [a | b] and dh of the routed rows in the FP8 input side's scratch (the
 // shared expert's rows follow them).

@@ -501,6 +501,18 @@ moe_status_t moe_transpose_weights_fp8(const void* w_q, const float* w_scales, i
                                                 as_stream(stream)));
 }
 
+moe_status_t moe_quantize_act_fp8_128x1(const void* x, int32_t rows, int32_t cols, void* q,
+                                        float* scales, void* stream) {
+  if (x == nullptr || q == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;
+  if (rows < 1 || cols < 1) return MOE_ERR_INVALID_ARG;
+  if (cols % 128 != 0 || cols / 128 > 65535) return MOE_ERR_SHAPE;
+  const void* ptrs[] = {x, q, scales};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  return from_cuda(launch_quantize_act_128x1(x, rows, cols, static_cast<uint8_t*>(q), scales,
+                                             as_stream(stream)));
+}
+
 moe_status_t moe_experts_backward_input_fp8(
     const moe_cfg_t* cfg, const void* x_perm, const float* x_perm_scales, const void* x_q,
     const float* x_q_scales, const int32_t* offsets, const void* w13, const float* w13_scales,

@@ -230,6 +230,40 @@ def test_fp8_kept_ab_matches_recomputed(shape):
         assert rel_frobenius(g, host(r)) < 2e-3, (name, rel_frobenius(g, host(r)))
 
 
+def test_fp8_128x1_quantiser_is_exact():
+    """moe_quantize_act_fp8_128x1 (the quantiser of Wgrad's operands) against
+    the oracle's 128 x 1 tiles, codes and scales bit for bit: a ragged last
+    tile, an all-zero column, outlier rows, and a column whose scale is 1
+    holding values exactly on E4M3 rounding midpoints and one bf16 step
+    either side (the quotients the reciprocal path hands to the exact
+    division)."""
+    rng = np.random.default_rng(12)
+    rows, cols = 300, 384
+    x = rng.standard_normal((rows, cols)) * np.exp(rng.standard_normal(cols))[None, :]
+    x[rng.integers(0, rows, 6)] *= 40.0
+    x[:, 5] = 0.0
+    # column 7: amax 448 in every tile (scale 1), then midpoints of E4M3 steps
+    grid = np.array([1.0, 1.125, 1.25, 1.375, 1.5, 1.625, 1.75, 1.875, 2.0])
+    mids = np.concatenate([(grid[:-1] + grid[1:]) / 2 * 2.0 ** e for e in range(-6, 8)])
+    mb = torch.tensor(mids, dtype=torch.float32).bfloat16()  # exact: 5 significant bits
+    step = [(mb.view(torch.int16) + k).view(torch.bfloat16).float().numpy() for k in (-1, 1)]
+    col = np.resize(np.concatenate([mids, step[0], step[1]]), rows)
+    col[::128] = 448.0
+    x[:, 7] = col
+    xb = torch.tensor(x, dtype=torch.float32).bfloat16()
+    xf = xb.float().numpy()
+    P = (rows + 127) // 128 * 128
+    q = torch.empty(P, cols, dtype=torch.float8_e4m3fn, device=DEV)
+    sc = torch.empty(P // 128, cols, dtype=torch.float32, device=DEV)
+    moe.moe_quantize_act_fp8_128x1(xb.to(DEV), q, sc)
+    assert moe.moe_get_device_error() == 0
+    rq, rs = quantize_act_128x1(xf)
+    assert np.array_equal(host(sc), np.asarray(rs, np.float32)), "scales"
+    got = q.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got[:rows], rq), "codes"
+    assert not got[rows:].any(), "padding rows"
+
+
 def test_fp8_weight_transpose_is_exact():
     """The transposed copies hold the forward's codes and block scales,
     transposed: nothing is quantised again."""
