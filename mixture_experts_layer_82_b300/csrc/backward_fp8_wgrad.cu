@@ -148,26 +148,6 @@ __device__ __forceinline__ float4 staged_quad(const uint8_t* t, int r, int l, bo
                      h.w * (av.w * sg.w));
 }
 
-// E4M3 codes of fl32(a / sa) and fl32(b / sb) (nearest even, saturating),
-// given ra = fl32(1 / sa) and rb = fl32(1 / sb).  q = fl32(a ra) is within
-// 2.5 fp32 ulps of fl32(a / sa): ra carries half an ulp of relative error
-// and the product another half, and the quotient itself is rounded by half
-// an ulp.  The conversion to E4M3 is monotonic, so when q widened by 4 ulps
-// either way gives the same code, that is the code of fl32(a / sa); only a
-// quotient near an E4M3 rounding boundary takes the exact division.
-__device__ __forceinline__ uint32_t e4m3x2_of_quotients(float a, float b, float sa, float sb,
-                                                        float ra, float rb) {
-  const float qa = a * ra, qb = b * rb;
-  const float ea = fabsf(qa) * 0x1p-21f, eb = fabsf(qb) * 0x1p-21f;
-  const __nv_fp8x2_storage_t lo =
-      __nv_cvt_float2_to_fp8x2(make_float2(qa - ea, qb - eb), __NV_SATFINITE, __NV_E4M3);
-  const __nv_fp8x2_storage_t hi =
-      __nv_cvt_float2_to_fp8x2(make_float2(qa + ea, qb + eb), __NV_SATFINITE, __NV_E4M3);
-  if (lo == hi) return lo;
-  return __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, sa), __fdiv_rn(b, sb)), __NV_SATFINITE,
-                                  __NV_E4M3);
-}
-
 // One block per (128-row tile of the padded layout, 128 columns).  Thread
 // 0 copies the tile's source boxes into shared memory (rows past the
 // segment are copied too and zeroed here); warp w then forms rows

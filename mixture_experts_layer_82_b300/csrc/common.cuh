@@ -528,6 +528,26 @@ __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// E4M3 codes of fl32(a / sa) and fl32(b / sb) (nearest even, saturating),
+// given ra = fl32(1 / sa) and rb = fl32(1 / sb).  q = fl32(a ra) is within
+// 2.5 fp32 ulps of fl32(a / sa): ra carries half an ulp of relative error
+// and the product another half, and the quotient itself is rounded by half
+// an ulp.  The conversion to E4M3 is monotonic, so when q widened by 4 ulps
+// either way gives the same code, that is the code of fl32(a / sa); only a
+// quotient near an E4M3 rounding boundary takes the exact division.
+__device__ __forceinline__ uint32_t e4m3x2_of_quotients(float a, float b, float sa, float sb,
+                                                        float ra, float rb) {
+  const float qa = a * ra, qb = b * rb;
+  const float ea = fabsf(qa) * 0x1p-21f, eb = fabsf(qb) * 0x1p-21f;
+  const __nv_fp8x2_storage_t lo =
+      __nv_cvt_float2_to_fp8x2(make_float2(qa - ea, qb - eb), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi =
+      __nv_cvt_float2_to_fp8x2(make_float2(qa + ea, qb + eb), __NV_SATFINITE, __NV_E4M3);
+  if (lo == hi) return lo;
+  return __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, sa), __fdiv_rn(b, sb)), __NV_SATFINITE,
+                                  __NV_E4M3);
+}
+
 // Register budget of a warpgroup, moved between warpgroups after launch.
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }

@@ -60,12 +60,12 @@ __device__ __forceinline__ float fp8_scale_of(float amax) {
   return amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
+// E4M3 codes of fl32(a / scale) .. fl32(d / scale), packed (the exact
+// quotients' codes, through the reciprocal with its exactness check).
 __device__ __forceinline__ uint32_t quant4_e4m3(float a, float b, float c, float d, float scale) {
-  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-      make_float2(__fdiv_rn(a, scale), __fdiv_rn(b, scale)), __NV_SATFINITE, __NV_E4M3);
-  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-      make_float2(__fdiv_rn(c, scale), __fdiv_rn(d, scale)), __NV_SATFINITE, __NV_E4M3);
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  const float r = __frcp_rn(scale);
+  return e4m3x2_of_quotients(a, b, scale, scale, r, r) |
+         (e4m3x2_of_quotients(c, d, scale, scale, r, r) << 16);
 }
 
 // E4M3 codes of a * rs ... d * rs (rs: a reciprocal scale), packed.
