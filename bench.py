@@ -508,6 +508,8 @@ def measure_ours(args, shape, world, rank, local, cpu_baseline):
     K = args.steps
     ev_exp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(K)]
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
@@ -515,13 +517,16 @@ def measure_ours(args, shape, world, rank, local, cpu_baseline):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(K):
+        ev_step[i][0].record(stream)
         layer.forward(x, expert_events=ev_exp[i], load_group=lg, gated=gated)
+        ev_step[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     exp_ms = [a.elapsed_time(b) for a, b in ev_exp]
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
     status = moe.moe_get_device_error()
     if status != 0:
         raise RuntimeError(f"device error status {status} in the timed region")
@@ -641,6 +646,10 @@ def measure_ours(args, shape, world, rank, local, cpu_baseline):
                    "l2": "inputs larger than L2: every step streams all expert weights "
                          f"({(3 * shape.d * shape.inter * (shape.E + shape.n_shared)) * (1 if shape.dtype == 'fp8' else 2) / 1e9:.1f} GB)"},
         "layer_tflops": layer_flops(shape) * world * K / (total_ms * 1e-3) / 1e12,
+        # each step's own events (this rank): the median and the best of the K steps
+        "per_step": {"layer_ms_median": statistics.median(step_ms), "layer_ms_best": min(step_ms),
+                     "expert_ms_median": statistics.median(exp_ms), "expert_ms_best": min(exp_ms),
+                     "frac_at_best_expert_ms": roofline["frac"] * exp_mean / min(exp_ms)},
         "roofline": roofline,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
