@@ -209,6 +209,47 @@ def test_backward_calls_check_before_launching():
     assert lib.moe_experts_grouped_train(fp32, *p, big, a, ws, None) == 2
 
 
+def test_fp8_backward_calls_check_before_launching():
+    """The FP8 training calls: kind and shared-expert limits, NULL and
+    misaligned pointers, workspace sizes, the 128 x 1 quantiser's width."""
+    lib = moe.library()
+    a = 0x100000
+    f8 = _base(dtype="fp8", n_shared=1)
+    f8c = ctypes.byref(f8.c())
+    bf = ctypes.byref(_base().c())
+    two = ctypes.byref(_base(dtype="fp8", n_shared=2).c())
+    ws = moe.moe_backward_workspace_bytes(f8)
+    big = moe.moe_workspace_bytes(f8)
+    # training forward keeping [a | b]: kind, N_s <= 1, bws size and alignment
+    p = [a] * 16
+    assert lib.moe_experts_grouped_train_fp8(bf, *p, big, a, ws, None) == 2
+    assert lib.moe_experts_grouped_train_fp8(two, *p, big, a, ws, None) == 2
+    assert lib.moe_experts_grouped_train_fp8(f8c, *p, big, None, ws, None) == 1
+    assert lib.moe_experts_grouped_train_fp8(f8c, *p, big, a + 8, ws, None) == 3
+    assert lib.moe_experts_grouped_train_fp8(f8c, *p, big, a, ws - 1, None) == 7
+    # Dgrad: kind, a missing weight transpose, misaligned dy, small workspace
+    p = [a] * 21
+    assert lib.moe_experts_backward_input_fp8(bf, *p, 0, a, ws, None) == 2
+    q = list(p); q[8] = None  # w2t
+    assert lib.moe_experts_backward_input_fp8(f8c, *q, 1, a, ws, None) == 1
+    q = list(p); q[17] = a + 4  # dy_perm
+    assert lib.moe_experts_backward_input_fp8(f8c, *q, 0, a, ws, None) == 3
+    assert lib.moe_experts_backward_input_fp8(f8c, *p, 0, a, 16, None) == 7
+    # Wgrad: kind, NULL dW2, the shared expert's dWs2, small workspace
+    p = [a] * 11
+    assert lib.moe_experts_backward_weights_fp8(bf, *p, a, ws, None) == 2
+    q = list(p); q[8] = None  # dw2
+    assert lib.moe_experts_backward_weights_fp8(f8c, *q, a, ws, None) == 1
+    q = list(p); q[10] = None  # dws2 with N_s = 1
+    assert lib.moe_experts_backward_weights_fp8(f8c, *q, a, ws, None) == 1
+    assert lib.moe_experts_backward_weights_fp8(f8c, *p, a, 16, None) == 7
+    # 128 x 1 quantiser: width, NULL, alignment, empty
+    assert lib.moe_quantize_act_fp8_128x1(a, 300, 200, a, a, None) == 2
+    assert lib.moe_quantize_act_fp8_128x1(None, 300, 256, a, a, None) == 1
+    assert lib.moe_quantize_act_fp8_128x1(a, 300, 256, a + 8, a, None) == 3
+    assert lib.moe_quantize_act_fp8_128x1(a, 0, 256, a, a, None) == 1
+
+
 def test_bias_update_takes_the_whole_batch_of_many_replicas():
     """Data-parallel replicas call moe_bias_update with T = world x T (the
     whole batch's mean load).  That T may exceed the 2^22 tokens one routing
