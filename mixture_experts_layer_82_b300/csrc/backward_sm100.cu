@@ -75,6 +75,7 @@ struct ClassDesc {
 struct Params {
   CUtensorMap a_map[2];  // [0] routed class, [1] shared class
   CUtensorMap b_map[2];
+  CUtensorMap out_map[2];  // Wgrad: the class's gradients [groups][m_dim][n_dim], box 1 x 32 x 64
   ClassDesc cls[2];
   const int32_t* offsets;
   int n_rows;  // T * K: permuted rows, the bound of every segment
@@ -87,7 +88,7 @@ struct Params {
 
 struct Smem {
   // Wgrad epilogue: per epilogue warp, 32 rows x 64 bf16 columns (128-byte
-  // rows, 16-byte pieces XOR-swizzled by the row) on their way to global
+  // rows, 16-byte pieces XOR-swizzled by the row) on their way to a TMA store
   alignas(16) uint8_t stage_out[4][32 * 128];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -377,18 +378,19 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
       const int n_base = tl.nt * BN;
       if (KIND == WG) {
         // The weight-gradient tile is written whole (64 KiB per tile, about
-        // as much time as its MMAs take), so the stores are coalesced: per
-        // 64-column chunk each lane puts its row into the warp's staging
-        // rows (16-byte pieces XOR-swizzled by the row), then the warp
-        // writes 4 full 128-byte rows per store instruction.  The TMEM
-        // loads of the next chunk are in flight meanwhile.  m_dim is a
-        // multiple of 128, so every row is inside the matrix.
+        // as much time as its MMAs take): per 64-column chunk each lane puts
+        // its row into the warp's staging rows (the 128-byte swizzle), and
+        // lane 0 hands the 32 x 64 chunk to a TMA store through the class's
+        // 3-D map of the gradients.  The staging rows are reused once the
+        // warp's previous store has read them; the TMEM loads of the next
+        // chunk are in flight meanwhile.  m_dim is a multiple of 128, so
+        // every row is inside the matrix.
         const bool empty = tl.rows == 0;
         uint8_t* stg = s.stage_out[q];
-        __nv_bfloat16* obase = cd.out + cd.out_group_stride * tl.j +
-                               static_cast<size_t>(tl.mt * BM + q * 32) * p.n_dim;
-        const int cc = lane & 7;
         auto put = [&](const float (&x0)[32], const float (&x1)[32], int c) {
+          // the warp's previous store has read the staging rows
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float* x = j < 4 ? x0 + 8 * j : x1 + 8 * (j - 4);
@@ -396,16 +398,12 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
                                        pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
             *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
           }
+          fence_proxy_async_smem();
           __syncwarp();
-          const int col = n_base + c * 64 + cc * 8;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = i * 4 + (lane >> 3);
-            const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((cc ^ (rr & 7)) << 4));
-            if (col < p.n_dim)
-              *reinterpret_cast<uint4*>(obase + static_cast<size_t>(rr) * p.n_dim + col) = w;
+          if (lane == 0 && n_base + c * 64 < p.n_dim) {  // (chunks past the matrix: no store)
+            tma_store_3d(&p.out_map[tl.cls], stg, n_base + c * 64, tl.mt * BM + q * 32, tl.j);
+            bulk_commit();
           }
-          __syncwarp();
         };
         float a0[32], a1[32], b0[32], b1[32];
         if (empty) {
@@ -491,6 +489,8 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.tempty[acc]);
     }
+    // the warp's last gradient stores have completed
+    if (KIND == WG && lane == 0) bulk_wait_all();
   }
   __syncthreads();
   if (warp == 1) {
@@ -628,6 +628,17 @@ cudaError_t launch_experts_bwd_input_bf16(const ExpertsBwdArgs& a, cudaStream_t 
   return launch_bwd_gemm<DG_PLAIN>(q, st);
 }
 
+// Wgrad output of a class: `groups` matrices [m, n] bf16 seen as a 3-D map
+// with a 32-row x 64-column box (one epilogue warp's chunk, 128-byte swizzle).
+static CUresult encode_wgrad_out(CUtensorMap* m, void* base, int rows, int cols, int groups) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                            static_cast<uint64_t>(groups)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(cols) * 2, static_cast<uint64_t>(rows) * cols * 2};
+  const uint32_t box[3] = {64, 32, 1};
+  return encode_tensor_map_nd(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, 3, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 cudaError_t launch_experts_bwd_weights_bf16(const ExpertsBwdArgs& a, cudaStream_t st) {
   using namespace bwdgemm;
   const moe_cfg_t& c = *a.cfg;
@@ -656,6 +667,11 @@ cudaError_t launch_experts_bwd_weights_bf16(const ExpertsBwdArgs& a, cudaStream_
   const size_t mat2 = static_cast<size_t>(d) * I;
   p.cls[0] = ClassDesc{0, 0, 0, 0, static_cast<__nv_bfloat16*>(a.dw2), 0, 0, mat2, nullptr, 0, 0};
   p.cls[1] = ClassDesc{0, 0, 0, I, static_cast<__nv_bfloat16*>(a.dws2), 0, 0, mat2, nullptr, 0, 0};
+  r = encode_wgrad_out(&p.out_map[0], a.dw2, d, I, c.E);
+  if (r == CUDA_SUCCESS)
+    r = has_shared ? encode_wgrad_out(&p.out_map[1], a.dws2, d, I, Ns) : CUDA_SUCCESS;
+  if (!has_shared) p.out_map[1] = p.out_map[0];
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   cudaError_t e = launch_bwd_gemm<WG>(p, st);
   if (e != cudaSuccess) return e;
 
@@ -679,6 +695,11 @@ cudaError_t launch_experts_bwd_weights_bf16(const ExpertsBwdArgs& a, cudaStream_
   q.cls[0] = ClassDesc{0, 0, 0, 0, static_cast<__nv_bfloat16*>(a.dw13), 0, 0, mat13, nullptr, 0, 0};
   q.cls[1] = ClassDesc{0, 0, 2 * I, 0, static_cast<__nv_bfloat16*>(a.dws13), 0, 0, mat13, nullptr,
                        0, 0};
+  r = encode_wgrad_out(&q.out_map[0], a.dw13, 2 * I, d, c.E);
+  if (r == CUDA_SUCCESS)
+    r = has_shared ? encode_wgrad_out(&q.out_map[1], a.dws13, 2 * I, d, Ns) : CUDA_SUCCESS;
+  if (!has_shared) q.out_map[1] = q.out_map[0];
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   return launch_bwd_gemm<WG>(q, st);
 }
 
