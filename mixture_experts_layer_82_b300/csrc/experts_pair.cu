@@ -32,13 +32,16 @@
 // copies complete on the even CTA's full barrier, which expects both CTAs'
 // bytes.  The even CTA's MMA thread issues the pair MMAs; its commits arrive
 // on the empty and accumulator-full barriers of both CTAs.  Each CTA's
-// epilogue drains its own TMEM and arrives on the even CTA's
-// accumulator-empty barrier (eight warps in all).  Every wait is bounded.
+// epilogue drains its own TMEM; the even CTA's four warps arrive on its
+// accumulator-empty barrier, the odd CTA's on a local one, which a relay
+// thread passes on with one cluster-scope arrival (a warp's own
+// cluster-scope release would wait for its outstanding output stores).
+// Every wait is bounded.
 //
 // Roles (224 threads, one CTA per SM, clusters of two): warps 0 and 6 TMA
 // producers (alternate stages of a 6-stage ring of 32 KiB), warp 1 TMEM
-// allocation (both CTAs) and the MMA thread (even CTA), warps 2..5 the
-// epilogue.
+// allocation (both CTAs), the MMA thread (even CTA) or the relay (odd CTA),
+// warps 2..5 the epilogue.
 #include <algorithm>
 
 #include "common.cuh"
@@ -58,7 +61,8 @@ struct Smem2 {
   uint64_t full[P2_STAGES];   // even CTA: both CTAs' copies of the stage have landed
   uint64_t empty[P2_STAGES];  // both CTAs: the pair MMAs have read the stage
   uint64_t tfull[2];          // both CTAs: the accumulator holds the tile
-  uint64_t tempty[2];         // even CTA: both epilogues have drained it (8 warps)
+  uint64_t tempty[2];         // even CTA: both epilogues have drained it (4 local warps + 1 relay)
+  uint64_t tdrained[2];       // odd CTA: its 4 epilogue warps have drained it
   uint64_t done;
   uint32_t tmem_base;
   int abort;
@@ -160,7 +164,11 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_pair_kernel(const __g
       if (MODE == GATEUP) tma_prefetch_desc(&p.b_mix[i]);
     }
     for (int i = 0; i < P2_STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&s.tfull[i], 1); mbar_init(&s.tempty[i], 8); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 5);
+      mbar_init(&s.tdrained[i], 4);
+    }
     mbar_init(&s.done, 1);
     s.abort = 0;
     fence_mbarrier_init();
@@ -245,6 +253,21 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_pair_kernel(const __g
         mbar_wait_drain(&s.empty[par + 2 * (j % HALF_RING)], (j / HALF_RING) & 1u);
       }
     }
+  } else if (warp == 1 && rank != 0) {
+    // ------------------------------------------- relay (odd CTA, warp 1)
+    // Once the odd CTA's four epilogue warps have drained an accumulator
+    // (CTA-scope arrivals), one cluster-scope arrival tells the even CTA's
+    // MMA thread; this thread has no stores of its own to wait for.
+    if (lane == 0) {
+      const uint32_t tempty_even0 = cluster_addr(&s.tempty[0], 0);
+      const uint32_t tempty_even1 = cluster_addr(&s.tempty[1], 0);
+      int it = 0;
+      for (int t = w_first; t < total; t += w_step, ++it) {
+        const int acc = it & 1;
+        if (!mbar_wait(&s.tdrained[acc], static_cast<uint32_t>(it >> 1) & 1u, abort_flag)) break;
+        mbar_arrive_cluster(acc ? tempty_even1 : tempty_even0);
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------- MMA (even CTA only)
     if (lane == 0 && rank == 0) {
@@ -286,8 +309,6 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_pair_kernel(const __g
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const uint32_t tempty_even0 = cluster_addr(&s.tempty[0], 0);
-    const uint32_t tempty_even1 = cluster_addr(&s.tempty[1], 0);
     int it = 0;
     for (int t = w_first; t < total; t += w_step, ++it) {
       const Tile2 tl = decode_tile2<MODE>(p, s, t);
@@ -368,7 +389,9 @@ __global__ void __launch_bounds__(THREADS, 1) experts_bf16_pair_kernel(const __g
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc ? tempty_even1 : tempty_even0);
+      // (CTA scope: the even CTA's warps arrive on its own barrier, the odd
+      // CTA's on theirs, which warp 1 relays)
+      if (lane == 0) mbar_arrive(rank == 0 ? &s.tempty[acc] : &s.tdrained[acc]);
     }
   }
   __syncthreads();
