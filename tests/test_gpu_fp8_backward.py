@@ -160,6 +160,9 @@ def _check_experts(L, layer, experts, off):
         dy = host(layer.dy_perm[lo:hi]).astype(np.float64)
         r = fp8_swiglu_ffn_backward(qx, sx, host(L["w13"][e]), host(L["w2"][e]), dy)
         _check_wgrad(got, r, qx, sx, dy, f"expert {e}")
+        # the same expert's input gradient (Dgrad) on its rows
+        assert_close(host(layer.dx_perm[lo:hi]), r["du"], TOL_FP8, f"dx_perm of expert {e}",
+                     row_tol=ROW_TOL_FP8_BWD)
         g2.append(got[0]); g13.append(got[1]); r2.append(r["dw2"]); r13.append(r["dw13"])
     return [np.concatenate(v) for v in (g2, r2, g13, r13)]
 
@@ -185,9 +188,9 @@ def test_fp8_wgrad_matches_oracle(shape):
 
 def test_fp8_wgrad_full_size_on_sampled_experts():
     """The FP8 layer at its full size (T = 8192, d = 7168, 256 experts, one
-    shared): the oracle recomputes the weight gradients of four experts, the
-    most loaded, one whose rows fit one 128-row tile, one with a ragged last
-    tile over several tiles, and the last expert."""
+    shared): the oracle recomputes the weight and input gradients of four
+    experts, the most loaded, one whose rows fit one 128-row tile, one with
+    a ragged last tile over several tiles, and the last expert."""
     shape = CONFIGS["v3_fp8"]
     L, layer, dout, dx = _run(shape)
     off = host(layer.offsets)
