@@ -42,6 +42,11 @@ SHAPES = [
     shape_with(CONFIGS["v3_fp8"], T=4096, d=2048, E=64, n_groups=8, topk_groups=4, k=6,
                n_shared=2, inter=1408, route_scale=1.0, router="gaussian",
                outlier_channels=20),
+    # segments averaging 256 rows: several M tiles per expert with ragged
+    # tails; d % 256 == 128 and I % 256 == 128 (the last N tile of each GEMM
+    # half outside), one shared expert
+    shape_with(CONFIGS["v3_fp8"], T=1024, d=640, E=8, n_groups=4, topk_groups=2, k=2,
+               n_shared=1, inter=384, route_scale=1.0, router="gaussian", outlier_channels=7),
 ]
 
 

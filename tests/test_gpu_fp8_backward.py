@@ -57,6 +57,10 @@ SHAPES = [
     # no shared expert; I not a multiple of 256 (the last N tile half outside)
     shape_with(CONFIGS["v3_fp8"], T=200, d=640, E=8, n_groups=4, topk_groups=2, k=2, n_shared=0,
                inter=384, route_scale=1.0, router="gaussian", outlier_channels=7),
+    # segments averaging 256 rows (several M tiles per expert, ragged
+    # tails), with a shared expert
+    shape_with(CONFIGS["v3_fp8"], T=1024, d=512, E=8, n_groups=4, topk_groups=2, k=2, inter=256,
+               route_scale=1.0, router="gaussian", outlier_channels=5),
 ]
 
 
@@ -219,7 +223,7 @@ def test_fp8_backward_is_deterministic():
     assert moe.moe_get_device_error() == 0
 
 
-@pytest.mark.parametrize("shape", [SHAPES[0], SHAPES[2]],
+@pytest.mark.parametrize("shape", [SHAPES[0], SHAPES[2], SHAPES[3]],
                          ids=lambda s: f"T{s.T}-d{s.d}-E{s.E}-I{s.inter}-Ns{s.n_shared}")
 def test_fp8_kept_ab_matches_recomputed(shape):
     """The training forward's [a | b] (the gate/up promotion's fp32 sums,
