@@ -269,12 +269,11 @@ __device__ __forceinline__ bool promote_block(Smem& s, float (&acc)[128], uint32
   if (!mbar_wait(&s.pfull[buf], (pc >> 1) & 1u, abort_flag)) return false;
   tc_fence_after();
   const uint32_t taddr = lane_addr + static_cast<uint32_t>(buf * PN);
-  // Gate/up: the half's 64 gate columns then its 64 up columns, in four
-  // batches of 16 + 16; down: the half's 128 columns in two batches of
-  // 32 + 32 (what the register budget allows without spilling).  The
-  // partial goes back to the MMA issuer as soon as the last batch is in
-  // registers (tcgen05.wait::ld returns once the loads have completed),
-  // before that batch's FMAs.
+  // Two batches of 32 + 32 columns (what the register budget allows without
+  // spilling): gate/up 32 gate columns with their 32 up columns, down 64
+  // consecutive columns.  The partial goes back to the MMA issuer as soon
+  // as the last batch is in registers (tcgen05.wait::ld returns once the
+  // loads have completed), before that batch's FMAs.
   constexpr int NB = 2;  // batches
   constexpr int W = 128 / (2 * NB);           // columns per load
 #pragma unroll
@@ -458,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1) experts_fp8_kernel(const __grid_co
     // ------------------------------------------------- promotion + epilogue
     // The TMEM base and the tile count are read from shared memory again
     // here, so that no value computed before the role split (where the
-    // producer/MMA warpgroup's 56-register budget applies) is live in this
+    // producer/MMA warpgroup's 40-register budget applies) is live in this
     // warpgroup's loops.
     const uint32_t tmem_base_e = *reinterpret_cast<volatile uint32_t*>(&s.tmem_base);
     const int total_e = reinterpret_cast<volatile int*>(s.gstart)[s.n_groups];

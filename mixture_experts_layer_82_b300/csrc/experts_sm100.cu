@@ -23,10 +23,11 @@
 // Each CTA still holds whole A and B tiles and runs its own 128 x 256 MMAs;
 // what the pair saves is L2 reads (a stage reads 48 KiB from L2 per CTA,
 // 32 KiB when B is shared), not what each SM takes in (48 KiB a stage
-// either way); experts_pair.cu's pair MMAs lower that.  Cluster c takes units c, c + clusters, ...; inside a
-// group the M pair varies fastest, so the clusters running at the same time
-// share each weight tile through L2.  (The gathering gate/up GEMM keeps one
-// tile per CTA: its A rows come from gather warps, not TMA.)
+// either way); experts_pair.cu's pair MMAs lower that.  Cluster c takes
+// units c, c + clusters, ...; inside a group the M pair varies fastest, so
+// the clusters running at the same time share each weight tile through L2.
+// (The gathering gate/up GEMM keeps one tile per CTA: its A rows come from
+// gather warps, not TMA.)
 //
 // Roles (224 threads, one CTA per SM):
 //   warps 0, 6  TMA producers (even / odd stages): A and B tiles into a
